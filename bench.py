@@ -1,0 +1,398 @@
+#!/usr/bin/env python
+"""Benchmark of the split-KV attention forward on GB300.
+
+Default workload: long-context decode, B=1, Q=1, K=131072, H_q=H_kv=32,
+D=128, bf16 N(0,1) inputs, automatic split count (the split sweep workload of
+flash-attention PR "[Cute,Fwd,Sm100] Support q_stage=1 for inference",
+"Benchmarks").  One step = one pass of the whole path: the split partial
+kernel plus the combine kernel.  The metric is HBM throughput in TB/s with
+the bytes counted as that page counts them (K + V + Q + O at the storage
+width), divided by the device time of a step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload long_decode|gqa_decode|fp8_prefix|fp8_prefix_11k]
+                  [--num-splits S] [--kernel auto|simt|umma]
+
+With N > 1 (torchrun) every rank runs its own replica of the workload
+(independent problems: weak scaling, no collective on the data path) and
+rank 0 prints the aggregate.  `--impl reference` times the float64 CPU
+oracle on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from workloads import workload  # noqa: E402
+
+METRIC = "decode attn HBM TB/s (K=128K, Q=1) & varlen prefill TFLOPS, % of roofline"
+FALLBACK_HBM_GBS = 6800.0
+CSRC = os.path.join(ROOT, "split_kv_flashattention_gb300", "csrc")
+
+WORKLOADS = {
+    "long_decode": dict(name="long_decode", kw={},
+                        desc="long-context decode MHA: B=1, Q=1, K=131072, H_q=H_kv=32, D=128, bf16"),
+    "gqa_decode": dict(name="gqa_decode", kw={},
+                       desc="batched GQA decode varlen: B=32, Q=1, H_q=32, H_kv=8, D=128, "
+                            "K lengths U[1024,32768] seed 0, bf16"),
+    "fp8_prefix": dict(name="fp8_prefix", kw={"kv": 16384},
+                       desc="short cached-prefix FP8: B=1, Q=70, H=12, D_qk=192, D_v=128, KV=16384, e4m3"),
+    "fp8_prefix_11k": dict(name="fp8_prefix", kw={"kv": 11008},
+                           desc="short cached-prefix FP8: B=1, Q=70, H=12, D_qk=192, D_v=128, KV=11008, e4m3"),
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long_decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "umma"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    return ap.parse_args()
+
+
+def byte_counts(inp, ns):
+    """Algorithmic bytes: the metric's (K+V+Q+O at storage width) and the
+    partial kernel's (K+V+Q read, workspace or O+LSE written)."""
+    es = 1 if inp.dtype == "e4m3" else 2
+    tq, tk = inp.q.shape[0], inp.k.shape[0]
+    kv = tk * inp.h_kv * (inp.d_qk + inp.d_v) * es
+    q = tq * inp.h_q * inp.d_qk * es
+    o = tq * inp.h_q * inp.d_v * 2
+    metric = kv + q + o
+    if ns > 1:
+        partial = kv + q + ns * tq * inp.h_q * (inp.d_v + 1) * 4
+    else:
+        partial = kv + q + o + tq * inp.h_q * 4
+    return metric, partial
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(CSRC, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_tag, workload_name):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, or None when absent or taken on different kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload_name}.txt")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_hash = re.search(r"^source_hash:\s*(\S+)", text, re.M)
+    m_t = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+    if not m_hash or not m_t or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.error = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception as e:  # pragma: no cover
+            self.error = str(e)
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if self.error or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "note": self.error or "no nvidia-smi samples"}
+        inside = [p for t, p in self.samples if t0 <= t <= t1] or [p for _, p in self.samples]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        mx = [num(p[1]) for p in inside if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside)}
+
+
+def cpu_baseline(inp_cpu, budget_s=12.0, heads=2):
+    """The float64 oracle on `heads` query heads of the workload, repeated for
+    about budget_s seconds on the host cores."""
+    import oracle
+
+    group = inp_cpu.h_q // inp_cpu.h_kv
+    hs = list(range(heads))
+    kvs = sorted({h // group for h in hs})
+    q = inp_cpu.q[:, hs]
+    k = inp_cpu.k[:, kvs]
+    v = inp_cpu.v[:, kvs]
+    es = 1 if inp_cpu.dtype == "e4m3" else 2
+    tq, tk = q.shape[0], k.shape[0]
+    sample_bytes = (tk * len(kvs) * (inp_cpu.d_qk + inp_cpu.d_v) * es
+                    + tq * heads * (inp_cpu.d_qk * es + inp_cpu.d_v * 2))
+    reps, t_total = 0, 0.0
+    while t_total < budget_s or reps == 0:
+        t = time.perf_counter()
+        oracle.attention_forward(q, k, v, inp_cpu.cu_seqlens_q, inp_cpu.cu_seqlens_k,
+                                 heads, len(kvs), 0.0, False, -1, inp_cpu.descale_q,
+                                 inp_cpu.descale_k, inp_cpu.descale_v)
+        t_total += time.perf_counter() - t
+        reps += 1
+    return {"value": sample_bytes * reps / t_total / 1e12, "unit": "TB/s",
+            "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{heads} of {inp_cpu.h_q} query heads (all keys), float64 oracle, "
+                      f"{reps} repetitions in {t_total:.1f} s, numpy/BLAS default threads",
+            "seconds": round(t_total, 2)}
+
+
+def inp_host(inp):
+    import dataclasses
+    return dataclasses.replace(inp, q=inp.q.cpu(), k=inp.k.cpu(), v=inp.v.cpu())
+
+
+def run_reference(args, spec, rank):
+    if rank != 0:
+        return
+    inp = workload(spec["name"], **spec["kw"])
+    steps_t = []
+    cb = None
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(inp, budget_s=0.0, heads=1)
+        if i >= args.warmup:
+            steps_t.append(r)
+        cb = r
+    vals = [r["value"] for r in steps_t] or [cb["value"]]
+    value = statistics.median(vals)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": spec["desc"]},
+        "cpu_baseline": {"value": value, "unit": "TB/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": cb["sample"].split(",")[0] +
+                         ", one oracle call per step"},
+        "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    spec = WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, spec, rank)
+        return
+
+    import split_kv_flashattention_gb300 as fa
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    kernel_flag = {"auto": fa.FA_KERNEL_AUTO, "simt": fa.FA_KERNEL_SIMT,
+                   "umma": fa.FA_KERNEL_UMMA}[args.kernel]
+    inp = workload(spec["name"], device=str(dev), **spec["kw"])
+    q, k, v = inp.q, inp.k, inp.v
+    cq, ck = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev)
+    out_dtype = torch.bfloat16 if inp.dtype == "e4m3" else q.dtype
+    out = torch.empty((q.shape[0], inp.h_q, inp.d_v), dtype=out_dtype, device=dev)
+    lse = torch.empty((inp.h_q, q.shape[0]), dtype=torch.float32, device=dev)
+    ns, _ = fa.fa_plan(inp.batch, inp.max_seqlen_q, inp.h_q, inp.h_kv, args.num_splits)
+    ws_bytes = fa.fa_fwd_splitkv_workspace_size(inp.batch, inp.max_seqlen_q, inp.h_q, inp.h_kv,
+                                               inp.d_v, args.num_splits)
+    ws = torch.empty(max(ws_bytes, 16) // 4, dtype=torch.float32, device=dev) if ws_bytes else None
+    dq = dk = dv = None
+    if inp.dtype == "e4m3":
+        dq = torch.tensor([inp.descale_q], dtype=torch.float32, device=dev)
+        dk = torch.tensor([inp.descale_k], dtype=torch.float32, device=dev)
+        dv = torch.tensor([inp.descale_v], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def partial():
+        fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, inp.max_seqlen_q, out, lse, ws, 0.0, False, -1,
+                             args.num_splits, dq, dk, dv, kernel_flag | fa.FA_RUN_PARTIAL_ONLY,
+                             stream)
+
+    def combine():
+        if ns > 1:
+            fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, inp.max_seqlen_q, out, lse, ws, 0.0, False, -1,
+                                 args.num_splits, dq, dk, dv,
+                                 kernel_flag | fa.FA_RUN_COMBINE_ONLY, stream)
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    for _ in range(args.warmup):
+        partial()
+        combine()
+    torch.cuda.synchronize(dev)
+    if fa.fa_get_device_error(clear=True) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        partial()
+        ev[i][1].record(stream)
+        combine()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    err = fa.fa_get_device_error(clear=True)
+    if err != 0:
+        raise RuntimeError(f"device error {fa.fa_status_string(err)}")
+
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    partial_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    metric_bytes, partial_bytes = byte_counts(inp, ns)
+    value = world * metric_bytes / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end through the public call with host buffers
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    hq, hk, hv = (x.cpu().pin_memory() for x in (inp.q, inp.k, inp.v))
+    hcq, hck = inp.cu_seqlens_q.pin_memory(), inp.cu_seqlens_k.pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hcq, hck))
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        cq.copy_(hcq, non_blocking=True)
+        ck.copy_(hck, non_blocking=True)
+        fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, inp.max_seqlen_q, out, lse, ws, 0.0, False, -1,
+                             args.num_splits, dq, dk, dv, kernel_flag, stream)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    te = torch.tensor([e0.elapsed_time(e1) / e2e_steps], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
+    e2e_value = world * metric_bytes / (float(te.item()) * 1e-3) / 1e12
+
+    if rank == 0:
+        peak_gbs, peak_src = measured_peaks()
+        achieved_gbs = partial_bytes / (partial_ms * 1e-3) / 1e9
+        kern_tag = "simt_splitkv" if args.kernel in ("auto", "simt") else "umma_splitkv"
+        traffic = profiled_traffic(kern_tag, args.workload)
+        line = {
+            "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if inp.dtype == "bf16" else inp.dtype, "data": "synthetic",
+            "config": {"workload": spec["desc"], "num_splits": ns,
+                       "num_splits_requested": args.num_splits, "kernel": args.kernel,
+                       "l2": "inputs larger than L2 (K+V %.2f GB)" % (
+                           (inp.k.numel() + inp.v.numel()) * inp.k.element_size() / 1e9),
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak_gbs,
+                         "unit": "GB/s", "frac": achieved_gbs / peak_gbs,
+                         "peak_source": peak_src, "traffic": traffic,
+                         "kernel": "split partial kernel", "partial_ms": partial_ms,
+                         "algorithmic_bytes_per_launch": partial_bytes},
+            "e2e": {"value": e2e_value, "unit": "TB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": args.steps * (2 if ns > 1 else 1),
+            "clocks": clocks,
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(inp_host(inp))
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

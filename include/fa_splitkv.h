@@ -1,0 +1,185 @@
+/*
+ * fa_splitkv.h -- C ABI of the split-KV flash-attention forward library
+ * (libfa_splitkv.so) for NVIDIA GB300 (sm_103a).
+ *
+ * What it computes.  For every packed sequence b, query head h and query row
+ * i < Lq_b, over the keys j the mask allows,
+ *     s_j = scale * dq * dk * <Q[cu_q[b]+i, h, :], K[cu_k[b]+j, h/group, :]>
+ *     LSE = ln(sum_j exp(s_j))
+ *     O   = dv * sum_j exp(s_j - LSE) * V[cu_k[b]+j, h/group, :]
+ * i.e. softmax(Q K^T * scale) V together with its natural-log log-sum-exp
+ * (flash-attention PR "[Cute,Fwd,Sm100] Support q_stage=1 for inference",
+ * description and "Benchmarks": split-KV forward; aiter PR "[FlyDSL] Enable
+ * FP8 FMHA split-K for short cached-prefix queries": return_lse and FP8).
+ * The key range of each (sequence, KV head, query tile) is cut into
+ * num_splits parts processed by separate CTAs, each writing an fp32 partial
+ * output and LSE to a caller-provided workspace; a combine kernel merges the
+ * parts with LSE weights (aiter PR, timing note: "attention and split
+ * combine").  Rows that see no key get O = 0 and LSE = -inf.
+ *
+ * Layout (cutlass "Adds variable sequence lengths to the Hopper CuTe DSL FMHA
+ * example", section "Interface"): all tensors are packed along the token
+ * axis, batch 1, innermost dimension contiguous:
+ *     Q   [total_q, h_q,  d_qk]      K [total_k, h_kv, d_qk]
+ *     V   [total_k, h_kv, d_v ]      O [total_q, h_q,  d_v ]
+ *     LSE [h_q, total_q] float32 (natural log, includes the scale)
+ *     cu_seqlens_q, cu_seqlens_k: int32 [batch+1], exclusive prefix sums;
+ *     a fixed-length side is passed as uniform cu_seqlens.
+ * GQA/MQA: h_q = group * h_kv, query head h reads KV head h / group.
+ *
+ * Masks (cutlass PR, section "Tests"): causal = 1 is bottom-right aligned
+ * (query i sees keys j <= i + Lk - Lq); window_left >= 0 is a (window_left, 0)
+ * sliding window (keys i+Lk-Lq-window_left .. i+Lk-Lq, inclusive), which
+ * implies the causal right bound; window_left < 0 means no left bound.
+ *
+ * Memory and ownership.  Every pointer is caller-owned: q, k, v, cu_seqlens,
+ * out, lse, workspace and descales are DEVICE pointers of the current CUDA
+ * device.  The library allocates no device memory and never synchronises the
+ * stream; all work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ * default stream), so calls can be captured in a CUDA graph.  Tensor-map
+ * descriptors are encoded on the host per call.
+ *
+ * Alignment.  q, k, v, out and workspace must be 16-byte aligned and every
+ * token stride (h * d * element size) a multiple of 16 bytes (TMA rule).
+ *
+ * Errors.  Invalid arguments are reported synchronously as a negative
+ * fa_status before anything is launched.  Problems found on the device
+ * (cu_seqlens inconsistent with batch / total_* / max_seqlen_q, or a
+ * pipeline wait that timed out) skip the affected tiles and set a sticky
+ * device error word, read with fa_get_device_error().
+ */
+#ifndef FA_SPLITKV_H
+#define FA_SPLITKV_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { FA_BF16 = 0, FA_FP16 = 1, FA_E4M3 = 2 } fa_dtype;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = -1,    /* bad pointer, size, alignment or value     */
+  FA_ERR_UNSUPPORTED = -2,    /* valid but not implemented (dtype / dims)  */
+  FA_ERR_WORKSPACE = -3,      /* workspace missing or too small            */
+  FA_ERR_CUDA = -4,           /* a CUDA runtime call failed                */
+  FA_ERR_DEVICE_TIMEOUT = -5, /* device: a pipeline wait ran out of time   */
+  FA_ERR_DEVICE_ARG = -6      /* device: cu_seqlens inconsistent with sizes */
+} fa_status;
+
+/* Kernel selection (flags argument of fa_fwd_splitkv_ex). */
+#define FA_KERNEL_AUTO 0 /* by rows per KV head: CUDA-core for few, tcgen05 else */
+#define FA_KERNEL_SIMT 1 /* CUDA-core streaming kernel                          */
+#define FA_KERNEL_UMMA 2 /* tcgen05 tensor-core kernel                          */
+#define FA_KERNEL_MASK 3
+/* Stage selection (flags, OR-ed with the kernel choice).  By default a call
+ * launches the partial kernel and, when the split count is > 1, the combine.
+ * PARTIAL_ONLY launches only the partial kernel (which writes the workspace,
+ * or O/LSE directly when the split count is 1); COMBINE_ONLY launches only the
+ * combine over a workspace written by an earlier PARTIAL_ONLY call with the
+ * same arguments.  Used to time the two kernels separately. */
+#define FA_RUN_PARTIAL_ONLY 4
+#define FA_RUN_COMBINE_ONLY 8
+
+/*
+ * fa_fwd_splitkv_ex -- split-KV attention forward (flash-decoding).
+ *
+ *  q, k, v        device inputs, layouts above, element type in_dtype.
+ *  cu_seqlens_q/k device int32 [batch+1].
+ *  batch          number of sequences (>= 0; 0 is a no-op).
+ *  total_q/total_k rows of the packed Q/O and K/V buffers; cu_seqlens_q[batch]
+ *                 must not exceed total_q, nor cu_seqlens_k[batch] total_k.
+ *                 TMA reads never go past these rows (zero fill beyond).
+ *  max_seqlen_q   largest Lq_b (sizes the tile grid and the workspace).
+ *  h_q, h_kv      query and key/value heads, h_q % h_kv == 0, h_q/h_kv <= 128.
+ *  d_qk, d_v      head dims: (64,64) or (128,128) for bf16/fp16;
+ *                 (128,128) or (192,128) for e4m3.
+ *  scale          softmax scale; <= 0 selects 1/sqrt(d_qk) (cutlass PR,
+ *                 "Implementation": the default scale uses the head dim).
+ *  causal, window_left  masks, see above.
+ *  num_splits     0 = automatic (fa_plan), else 1..128 splits of the key range.
+ *  out            device [total_q, h_q, d_v] of out_dtype (bf16 or fp16);
+ *                 rows of sequences are written, other rows are untouched.
+ *  lse            device float32 [h_q, total_q] or NULL.
+ *  workspace      device scratch of >= fa_fwd_splitkv_workspace_size(...)
+ *                 bytes when the resolved split count is > 1 (else may be NULL);
+ *                 contents need no initialisation and are clobbered.
+ *  workspace_bytes size of workspace (checked).
+ *  in_dtype, out_dtype  FA_BF16 / FA_FP16 / FA_E4M3 inputs; out is bf16 or
+ *                 fp16 (equal to in_dtype for 16-bit inputs).
+ *  descale_q/k/v  device float32 scalars, required for FA_E4M3 inputs
+ *                 (per-tensor dequantisation factors), ignored otherwise.
+ *  flags          FA_KERNEL_* selection, optionally OR FA_RUN_*_ONLY.
+ *  stream         cudaStream_t.
+ * Returns FA_OK or a negative fa_status.
+ */
+FA_API int fa_fwd_splitkv_ex(const void* q, const void* k, const void* v, const int* cu_seqlens_q,
+                      const int* cu_seqlens_k, int batch, int total_q, int total_k,
+                      int max_seqlen_q, int h_q, int h_kv, int d_qk, int d_v, float scale,
+                      int causal, int window_left, int num_splits, void* out, float* lse,
+                      void* workspace, size_t workspace_bytes, int in_dtype, int out_dtype,
+                      const float* descale_q, const float* descale_k, const float* descale_v,
+                      int flags, void* stream);
+
+/* bf16 in / bf16 out shorthand of fa_fwd_splitkv_ex with automatic kernel
+ * selection; the workspace is trusted to be large enough. */
+FA_API int fa_fwd_splitkv(const void* q, const void* k, const void* v, const int* cu_seqlens_q,
+                   const int* cu_seqlens_k, int batch, int total_q, int total_k,
+                   int max_seqlen_q, int h_q, int h_kv, int d_qk, int d_v, float scale,
+                   int causal, int window_left, int num_splits, void* out, float* lse,
+                   void* workspace, void* stream);
+
+/* Bytes of workspace fa_fwd_splitkv_ex needs for these sizes: the fp32
+ * partial outputs [ns, batch*max_seqlen_q, h_q, d_v] followed by the partial
+ * LSEs [ns, batch*max_seqlen_q, h_q]; 0 when the resolved split count is 1.
+ * num_splits = 0 resolves the automatic count on the current device. Returns
+ * 0 for invalid sizes as well. */
+FA_API size_t fa_fwd_splitkv_workspace_size(int batch, int max_seqlen_q, int h_q, int h_kv, int d_v,
+                                     int num_splits);
+
+/*
+ * fa_plan -- the split planner (host only; no device work).
+ * units = batch * h_kv * ceil(max_seqlen_q * (h_q/h_kv) / 128) work units;
+ * explicit num_splits > 0 is clipped to 128; with no work or with
+ * units >= 2*num_sms the count is 1; otherwise it is the smallest ns in
+ * 1..128 whose wave efficiency units*ns / (ceil(units*ns/num_sms)*num_sms)
+ * reaches 0.9, else the first most efficient one.  num_sms <= 0 queries the
+ * current device.  Writes the split count and the unit count.
+ */
+FA_API int fa_plan(int batch, int max_seqlen_q, int h_q, int h_kv, int num_splits, int num_sms,
+            int* num_splits_out, int* units_out);
+
+/*
+ * fa_debug_split_ranges -- test hook: runs the device-side tile decode for a
+ * tile of `tile_queries` queries and writes, for every (m_block, b, split),
+ * the sequence-local key range [k0, k1) the kernels process (k1 <= k0 for an
+ * empty split) to ranges_out: device int32 [ceil(max_seqlen_q/tile_queries),
+ * batch, num_splits, 2].  Enqueued on stream.
+ */
+FA_API int fa_debug_split_ranges(const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                          int max_seqlen_q, int causal, int window_left, int num_splits,
+                          int tile_queries, int* ranges_out, void* stream);
+
+/* Sticky device error word of the current device (FA_OK if none).  Waits
+ * for the device to finish its work.  clear != 0 resets the word. */
+FA_API int fa_get_device_error(int clear);
+
+/* Human-readable name of an fa_status value (static string). */
+FA_API const char* fa_status_string(int status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+FA_API int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_SPLITKV_H */

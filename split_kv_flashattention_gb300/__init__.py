@@ -1,0 +1,197 @@
+"""Split-KV flash-attention forward for GB300 (sm_103a).
+
+Python binding of ``libfa_splitkv.so`` (C ABI in ``include/fa_splitkv.h``).
+The functions here only marshal arguments: they read shapes and device
+pointers off torch tensors and call the C entry points of the same name.
+Every step of the computation runs in the library's CUDA kernels; there is
+no fallback.  If the library has not been built the first call raises
+``FaLibraryMissing``.
+
+Build:  ``python -m split_kv_flashattention_gb300.build``
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "FaError", "FaLibraryMissing", "library", "fa_fwd_splitkv_ex", "fa_fwd_splitkv",
+    "fa_fwd_splitkv_workspace_size", "fa_plan", "fa_debug_split_ranges",
+    "fa_get_device_error", "fa_status_string", "fa_version", "forward",
+    "FA_KERNEL_AUTO", "FA_KERNEL_SIMT", "FA_KERNEL_UMMA", "FA_RUN_PARTIAL_ONLY",
+    "FA_RUN_COMBINE_ONLY", "DTYPE_CODES",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libfa_splitkv.so")
+
+FA_KERNEL_AUTO, FA_KERNEL_SIMT, FA_KERNEL_UMMA = 0, 1, 2
+FA_RUN_PARTIAL_ONLY, FA_RUN_COMBINE_ONLY = 4, 8
+DTYPE_CODES = {torch.bfloat16: 0, torch.float16: 1, torch.float8_e4m3fn: 2}
+EXPORTED = (
+    "fa_fwd_splitkv_ex", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_plan",
+    "fa_debug_split_ranges", "fa_get_device_error", "fa_status_string", "fa_version",
+)
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {fa_status_string(status)} ({status})")
+        self.status = status
+
+
+class FaLibraryMissing(ImportError):
+    pass
+
+
+_lib = None
+
+_c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
+
+
+def library() -> ctypes.CDLL:
+    """The loaded C library (loaded on first use)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise FaLibraryMissing(
+            f"{LIB_PATH} is missing; build it with python -m split_kv_flashattention_gb300.build")
+    lib = ctypes.CDLL(LIB_PATH)
+    lib.fa_fwd_splitkv_ex.restype = _c_int
+    lib.fa_fwd_splitkv_ex.argtypes = [
+        _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+        _c_float, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_size, _c_int, _c_int, _vp, _vp, _vp,
+        _c_int, _vp]
+    lib.fa_fwd_splitkv.restype = _c_int
+    lib.fa_fwd_splitkv.argtypes = [
+        _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+        _c_float, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp]
+    lib.fa_fwd_splitkv_workspace_size.restype = _c_size
+    lib.fa_fwd_splitkv_workspace_size.argtypes = [_c_int] * 6
+    lib.fa_plan.restype = _c_int
+    lib.fa_plan.argtypes = [_c_int] * 6 + [ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]
+    lib.fa_debug_split_ranges.restype = _c_int
+    lib.fa_debug_split_ranges.argtypes = [_vp, _vp] + [_c_int] * 6 + [_vp, _vp]
+    lib.fa_get_device_error.restype = _c_int
+    lib.fa_get_device_error.argtypes = [_c_int]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_status_string.argtypes = [_c_int]
+    lib.fa_version.restype = _c_int
+    lib.fa_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise FaError(status, where)
+
+
+def fa_status_string(status: int) -> str:
+    return library().fa_status_string(int(status)).decode()
+
+
+def fa_version() -> int:
+    return library().fa_version()
+
+
+def fa_plan(batch: int, max_seqlen_q: int, h_q: int, h_kv: int, num_splits: int = 0,
+            num_sms: int = 0):
+    """(num_splits, units) chosen by the planner; num_sms <= 0 queries the device."""
+    ns, units = _c_int(0), _c_int(0)
+    _check(library().fa_plan(batch, max_seqlen_q, h_q, h_kv, num_splits, num_sms,
+                             ctypes.byref(ns), ctypes.byref(units)), "fa_plan")
+    return ns.value, units.value
+
+
+def fa_fwd_splitkv_workspace_size(batch: int, max_seqlen_q: int, h_q: int, h_kv: int, d_v: int,
+                                  num_splits: int = 0) -> int:
+    return int(library().fa_fwd_splitkv_workspace_size(batch, max_seqlen_q, h_q, h_kv, d_v,
+                                                       num_splits))
+
+
+def fa_get_device_error(clear: bool = False) -> int:
+    return library().fa_get_device_error(1 if clear else 0)
+
+
+def fa_debug_split_ranges(cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal: bool,
+                          window_left: int, num_splits: int, tile_queries: int, stream=None):
+    """Device-computed key ranges, int32 [m_blocks, batch, num_splits, 2]."""
+    batch = cu_seqlens_q.numel() - 1
+    m_blocks = -(-max_seqlen_q // tile_queries)
+    out = torch.full((m_blocks, batch, num_splits, 2), -1, dtype=torch.int32,
+                     device=cu_seqlens_q.device)
+    _check(library().fa_debug_split_ranges(_ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch,
+                                           max_seqlen_q, int(causal), window_left, num_splits,
+                                           tile_queries, _ptr(out), _stream(stream)),
+           "fa_debug_split_ranges")
+    return out
+
+
+def fa_fwd_splitkv_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, out, lse=None,
+                      workspace=None, scale: float = 0.0, causal: bool = False,
+                      window_left: int = -1, num_splits: int = 0, descale_q=None,
+                      descale_k=None, descale_v=None, flags: int = FA_KERNEL_AUTO,
+                      stream=None):
+    """Calls fa_fwd_splitkv_ex on torch CUDA tensors (shapes read from them).
+    flags: FA_KERNEL_* optionally OR-ed with FA_RUN_PARTIAL_ONLY/COMBINE_ONLY."""
+    total_q, h_q, d_qk = q.shape
+    total_k, h_kv, _ = k.shape
+    d_v = v.shape[2]
+    batch = cu_seqlens_q.numel() - 1
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = library().fa_fwd_splitkv_ex(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, total_q,
+        total_k, max_seqlen_q, h_q, h_kv, d_qk, d_v, float(scale), int(causal), int(window_left),
+        int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, DTYPE_CODES[q.dtype],
+        DTYPE_CODES[out.dtype], _ptr(descale_q), _ptr(descale_k), _ptr(descale_v), int(flags),
+        _stream(stream))
+    _check(st, "fa_fwd_splitkv_ex")
+
+
+def fa_fwd_splitkv(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, out, lse=None,
+                   workspace=None, scale: float = 0.0, causal: bool = False,
+                   window_left: int = -1, num_splits: int = 0, stream=None):
+    """Calls the bf16 shorthand entry point fa_fwd_splitkv."""
+    total_q, h_q, d_qk = q.shape
+    total_k, h_kv, _ = k.shape
+    st = library().fa_fwd_splitkv(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+        cu_seqlens_q.numel() - 1, total_q, total_k, max_seqlen_q, h_q, h_kv, d_qk, v.shape[2],
+        float(scale), int(causal), int(window_left), int(num_splits), _ptr(out), _ptr(lse),
+        _ptr(workspace), _stream(stream))
+    _check(st, "fa_fwd_splitkv")
+
+
+def forward(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, scale: float = 0.0,
+            causal: bool = False, window_left: int = -1, num_splits: int = 0,
+            descale_q=None, descale_k=None, descale_v=None, out_dtype=None,
+            kernel: int = FA_KERNEL_AUTO, stream=None):
+    """Allocates O, LSE and the workspace with torch, then calls
+    fa_fwd_splitkv_ex.  Returns (out [total_q, h_q, d_v], lse [h_q, total_q])."""
+    total_q, h_q, _ = q.shape
+    h_kv, d_v = k.shape[1], v.shape[2]
+    if out_dtype is None:
+        out_dtype = torch.bfloat16 if q.dtype == torch.float8_e4m3fn else q.dtype
+    out = torch.zeros((total_q, h_q, d_v), dtype=out_dtype, device=q.device)
+    lse = torch.full((h_q, total_q), float("nan"), dtype=torch.float32, device=q.device)
+    batch = cu_seqlens_q.numel() - 1
+    ws_bytes = fa_fwd_splitkv_workspace_size(batch, max_seqlen_q, h_q, h_kv, d_v, num_splits)
+    ws = torch.empty(max(ws_bytes, 16) // 4, dtype=torch.float32, device=q.device) if ws_bytes else None
+    fa_fwd_splitkv_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, out, lse, ws, scale,
+                      causal, window_left, num_splits, descale_q, descale_k, descale_v, kernel,
+                      stream)
+    return out, lse

@@ -1,0 +1,138 @@
+// LSE-weighted combine of split partials (flash-decoding's second kernel).
+//
+// aiter PR "[FlyDSL] Enable FP8 FMHA split-K for short cached-prefix
+// queries": the timed unit is "attention and split combine", with a per-call
+// fp32 workspace.  For every output row (token t, head h) one warp reads the
+// ns partial LSEs (lanes take splits s, s+32, ...), forms
+//     M = max_s lse_s,  w_s = exp(lse_s - M),  LSE = M + ln(sum_s w_s)
+// and accumulates O = sum_s (w_s / sum w) * O_s with 128-bit loads, lane l
+// owning columns [l*d_v/32, (l+1)*d_v/32).  Rows whose splits are all empty
+// (M = -inf) get O = 0 and LSE = -inf.
+#pragma once
+
+#include <math_constants.h>
+
+#include "fa_common.cuh"
+#include "fa_convert.cuh"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+template <int DV>
+__global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ FwdParams p) {
+  constexpr int DPL = DV / 32;
+  const int lane = threadIdx.x & 31;
+  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (gw >= (long long)p.slots * p.h_q) return;
+  const int slot = (int)(gw / p.h_q);
+  const int h = (int)(gw - (long long)slot * p.h_q);
+  const int b = slot / p.max_seqlen_q;
+  const int i = slot - b * p.max_seqlen_q;
+  SeqInfo sq;
+  if (!load_seq(p, b, sq)) return;  // reported by the partial kernel
+  if (i >= sq.lq) return;
+  const int t = sq.q0 + i;
+  const int ns = p.num_splits;
+  const size_t split_stride = (size_t)p.slots * p.h_q;
+  const size_t row0 = (size_t)slot * p.h_q + h;
+
+  constexpr float kLog2e = 1.4426950408889634f;
+  constexpr float kLn2 = 0.69314718055994531f;
+  float lv[kMaxSplits / 32];
+  float M = -CUDART_INF_F;
+#pragma unroll
+  for (int u = 0; u < kMaxSplits / 32; ++u) {
+    const int s = u * 32 + lane;
+    lv[u] = s < ns ? __ldg(p.ws_l + s * split_stride + row0) : -CUDART_INF_F;
+    M = fmaxf(M, lv[u]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+
+  float acc[DPL];
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+  float lse_out = -CUDART_INF_F;
+  if (M != -CUDART_INF_F) {
+    float w[kMaxSplits / 32];
+    float L = 0.f;
+#pragma unroll
+    for (int u = 0; u < kMaxSplits / 32; ++u) {
+      w[u] = fast_exp2((lv[u] - M) * kLog2e);  // empty split: exp2(-inf) = 0
+      L += w[u];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    const float inv = 1.f / L;
+    lse_out = M + __log2f(L) * kLn2;
+    const float* base = p.ws_o + row0 * DV + lane * DPL;
+#pragma unroll
+    for (int u = 0; u < kMaxSplits / 32; ++u) {
+      if (u * 32 >= ns) break;
+      const float wu = w[u] * inv;
+      const int n_here = min(32, ns - u * 32);
+#pragma unroll 4
+      for (int sl = 0; sl < n_here; ++sl) {
+        const float ws = __shfl_sync(0xffffffffu, wu, sl);
+        const float* src = base + (size_t)(u * 32 + sl) * split_stride * DV;
+        if (ws != 0.f) {
+          if constexpr (DPL % 4 == 0) {
+#pragma unroll
+            for (int e = 0; e < DPL; e += 4) {
+              const float4 v = __ldg(reinterpret_cast<const float4*>(src + e));
+              acc[e] = fmaf(ws, v.x, acc[e]);
+              acc[e + 1] = fmaf(ws, v.y, acc[e + 1]);
+              acc[e + 2] = fmaf(ws, v.z, acc[e + 2]);
+              acc[e + 3] = fmaf(ws, v.w, acc[e + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < DPL; e += 2) {
+              const float2 v = __ldg(reinterpret_cast<const float2*>(src + e));
+              acc[e] = fmaf(ws, v.x, acc[e]);
+              acc[e + 1] = fmaf(ws, v.y, acc[e + 1]);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  uint8_t* orow = static_cast<uint8_t*>(p.out) + ((size_t)t * p.h_q + h) * (size_t)DV * 2;
+  uint32_t pk[DPL / 2];
+#pragma unroll
+  for (int e = 0; e < DPL / 2; ++e) pk[e] = pack2(acc[2 * e], acc[2 * e + 1], p.out_dtype);
+  if constexpr (DPL == 8) {
+    *reinterpret_cast<uint4*>(orow + lane * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  } else if constexpr (DPL == 4) {
+    *reinterpret_cast<uint2*>(orow + lane * 8) = make_uint2(pk[0], pk[1]);
+  } else {
+    *reinterpret_cast<uint32_t*>(orow + lane * 4) = pk[0];
+  }
+  if (p.lse != nullptr && lane == 0) p.lse[(size_t)h * p.total_q + t] = lse_out;
+}
+
+// Test hook: the per-split key ranges the kernels compute, for a tile of
+// `tile_q` queries.  One thread per (m_block, b, split).
+__global__ void split_ranges_kernel(const int* cu_q, const int* cu_k, int batch, int max_seqlen_q,
+                                    int causal, int window_left, int ns, int tile_q, int m_blocks,
+                                    int* out) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long total = (long long)m_blocks * batch * ns;
+  if (idx >= total) return;
+  const int s = (int)(idx % ns);
+  const int b = (int)((idx / ns) % batch);
+  const int m = (int)(idx / ((long long)ns * batch));
+  const int lq = cu_q[b + 1] - cu_q[b];
+  const int lk = cu_k[b + 1] - cu_k[b];
+  int k0 = 0, k1 = 0;
+  const int i_lo = m * tile_q;
+  if (i_lo < lq) {
+    const int i_hi = min(lq - 1, i_lo + tile_q - 1);
+    tile_split_range(i_lo, i_hi, lq, lk, causal, window_left, ns, s, k0, k1);
+  }
+  out[2 * idx] = k0;
+  out[2 * idx + 1] = k1;
+}
+
+}  // namespace fa

@@ -1,0 +1,82 @@
+// Element conversions between the storage types (bf16, fp16, e4m3) and fp32.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "fa_common.cuh"
+
+namespace fa {
+
+template <int DT>
+struct Elem;
+template <>
+struct Elem<kBF16> {
+  static constexpr int size = 2;
+};
+template <>
+struct Elem<kFP16> {
+  static constexpr int size = 2;
+};
+template <>
+struct Elem<kE4M3> {
+  static constexpr int size = 1;
+};
+
+// One 32-bit word of packed elements -> floats (2 for 16-bit, 4 for e4m3).
+template <int DT>
+__device__ __forceinline__ void word_to_float(uint32_t w, float* f);
+
+template <>
+__device__ __forceinline__ void word_to_float<kBF16>(uint32_t w, float* f) {
+  f[0] = __uint_as_float(w << 16);
+  f[1] = __uint_as_float(w & 0xffff0000u);
+}
+
+template <>
+__device__ __forceinline__ void word_to_float<kFP16>(uint32_t w, float* f) {
+  __half2 h = *reinterpret_cast<__half2*>(&w);
+  float2 v = __half22float2(h);
+  f[0] = v.x;
+  f[1] = v.y;
+}
+
+template <>
+__device__ __forceinline__ void word_to_float<kE4M3>(uint32_t w, float* f) {
+  __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu),
+                                               __NV_E4M3);
+  __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16),
+                                               __NV_E4M3);
+  float2 a = __half22float2(*reinterpret_cast<__half2*>(&lo));
+  float2 b = __half22float2(*reinterpret_cast<__half2*>(&hi));
+  f[0] = a.x;
+  f[1] = a.y;
+  f[2] = b.x;
+  f[3] = b.y;
+}
+
+template <int DT>
+struct PerWord {
+  static constexpr int n = 4 / Elem<DT>::size;
+};
+
+// NW words -> NW * PerWord floats.
+template <int DT, int NWORDS>
+__device__ __forceinline__ void words_to_float(const uint32_t* w, float* f) {
+#pragma unroll
+  for (int i = 0; i < NWORDS; ++i) word_to_float<DT>(w[i], f + i * PerWord<DT>::n);
+}
+
+// Two floats -> one packed 16-bit pair for the output type (round to nearest).
+__device__ __forceinline__ uint32_t pack2(float a, float b, int out_dtype) {
+  if (out_dtype == kFP16) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+}  // namespace fa

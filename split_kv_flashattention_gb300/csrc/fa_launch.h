@@ -1,0 +1,39 @@
+// Internal launch interface between the C ABI (fa_api.cu) and the kernel
+// translation units.  Not part of the public header.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_common.cuh"
+
+namespace fa {
+
+// Rows per CTA the CUDA-core kernel can hold in registers for this dtype and
+// head dim (0 = unsupported).  Supported row tiles are 1, 2 and 4 up to it.
+int simt_max_rows(int dtype, int d_qk, int d_v);
+
+// Launch the CUDA-core split kernel.  grid = (row tiles, batch*h_kv, ns).
+cudaError_t launch_simt(int dtype, int d_qk, int d_v, int rows_per_tile, const FwdParams& p,
+                        const CUtensorMap& tmK, const CUtensorMap& tmV, dim3 grid,
+                        cudaStream_t stream);
+cudaError_t launch_simt_bf16(int d_qk, int d_v, int rt, const FwdParams& p, const CUtensorMap& tmK,
+                             const CUtensorMap& tmV, dim3 grid, cudaStream_t stream);
+cudaError_t launch_simt_fp16(int d_qk, int d_v, int rt, const FwdParams& p, const CUtensorMap& tmK,
+                             const CUtensorMap& tmV, dim3 grid, cudaStream_t stream);
+cudaError_t launch_simt_e4m3(int d_qk, int d_v, int rt, const FwdParams& p, const CUtensorMap& tmK,
+                             const CUtensorMap& tmV, dim3 grid, cudaStream_t stream);
+
+// Launch the split combine (one warp per output row).
+cudaError_t launch_combine(const FwdParams& p, cudaStream_t stream);
+
+// Test hook kernel for split ranges.
+cudaError_t launch_split_ranges(const int* cu_q, const int* cu_k, int batch, int max_seqlen_q,
+                                int causal, int window_left, int ns, int tile_q, int* out,
+                                cudaStream_t stream);
+
+// Sets the dynamic shared-memory limit of a kernel (once per kernel and
+// device; thread-safe).
+cudaError_t ensure_smem_attr(const void* kernel, int bytes);
+
+}  // namespace fa

@@ -1,0 +1,43 @@
+// Launch helper for the CUDA-core split kernel: picks the instantiation for
+// (dtype, d_qk, d_v, rows per tile).  Included by one translation unit per
+// input dtype so the instantiations compile in parallel.
+#pragma once
+
+#include "fa_launch.h"
+#include "fa_simt.cuh"
+
+namespace fa {
+
+// Stage ring sized so two CTAs fit on one SM (about 100 KB each).
+template <int DT, int DQK, int DV>
+struct SimtStages {
+  static constexpr int ES = Elem<DT>::size;
+  static constexpr int STAGE = (((DQK * ES + 127) / 128) + ((DV * ES + 127) / 128)) * 4096;
+  static constexpr int NS = (96 * 1024) / STAGE > 12 ? 12 : (96 * 1024) / STAGE;
+};
+
+template <int DT, int DQK, int DV, int RT>
+cudaError_t launch_simt_one(const FwdParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                            dim3 grid, cudaStream_t stream) {
+  constexpr int NW = 4;
+  constexpr int NS = SimtStages<DT, DQK, DV>::NS;
+  using C = SimtCfg<DT, DQK, DV, RT, NW, NS>;
+  auto kern = simt_splitkv_kernel<DT, DQK, DV, RT, NW, NS>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, C::NTHREADS, C::SMEM, stream>>>(p, tmK, tmV);
+  return cudaGetLastError();
+}
+
+template <int DT, int DQK, int DV, int RTMAX>
+cudaError_t launch_simt_dims(int rt, const FwdParams& p, const CUtensorMap& tmK,
+                             const CUtensorMap& tmV, dim3 grid, cudaStream_t stream) {
+  if (rt == 1) return launch_simt_one<DT, DQK, DV, 1>(p, tmK, tmV, grid, stream);
+  if (rt == 2) return launch_simt_one<DT, DQK, DV, 2>(p, tmK, tmV, grid, stream);
+  if constexpr (RTMAX >= 4) {
+    if (rt == 4) return launch_simt_one<DT, DQK, DV, 4>(p, tmK, tmV, grid, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -1,0 +1,258 @@
+"""GPU parity: the C-ABI CUDA path against the float64 oracle on the same
+seeded inputs.  Small cases are compared in full (several tiles and a ragged
+tail); the full-size workloads are compared on sampled heads in the launch
+configuration the benchmark times."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import split_kv_flashattention_gb300 as fa
+from gpu_harness import assert_close, reference, run_gpu
+from workloads import cu_seqlens, gqa_decode_lengths, make_inputs, workload
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = [fa.FA_KERNEL_SIMT]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    fa.library()
+    torch.cuda.init()
+
+
+# --------------------------------------------------------------- decode
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_tiny_decode_four_splits(kernel):
+    inp = workload("tiny_decode")
+    out, lse = run_gpu(inp, scale=0.125, num_splits=4, flags=kernel, ws_guard=64)
+    o_ref, l_ref = reference(inp, 0.125)
+    assert_close(inp, out, lse, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("ns", [0, 1, 2, 3, 7, 16, 128])
+def test_decode_mha_ragged_split_counts(kernel, ns):
+    inp = workload("long_decode", kv=5000, h=4)
+    out, lse = run_gpu(inp, num_splits=ns, flags=kernel, guard_rows=3, ws_guard=64)
+    o_ref, l_ref = reference(inp)
+    assert_close(inp, out, lse, o_ref, l_ref)
+    assert np.isnan(out[1:]).all() and np.isnan(lse[:, 1:]).all(), "guard rows written"
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_gqa_decode_varlen(kernel, group):
+    lens_k = [int(x) for x in np.random.default_rng(1).integers(1, 3000, size=6)]
+    lens_k[2] = 0
+    lens_k[4] = 1
+    inp = make_inputs([1] * 6, lens_k, 4 * group, 4, 128, 128, "bf16", seed=2)
+    out, lse = run_gpu(inp, flags=kernel)
+    o_ref, l_ref = reference(inp)
+    assert_close(inp, out, lse, o_ref, l_ref)
+    # the sequence without keys: O = 0, LSE = -inf
+    assert np.all(out[2] == 0) and np.all(np.isneginf(lse[:, 2]))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_head_dim_64(kernel, dtype):
+    inp = make_inputs([1, 2], [777, 1500], 8, 2, 64, 64, dtype, seed=3)
+    out, lse = run_gpu(inp, num_splits=5, flags=kernel)
+    o_ref, l_ref = reference(inp)
+    assert_close(inp, out, lse, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_lse_pointer_may_be_null(kernel):
+    inp = workload("long_decode", kv=3000, h=2)
+    out, lse = run_gpu(inp, num_splits=3, flags=kernel, with_lse=False)
+    o_ref, l_ref = reference(inp)
+    assert lse is None
+    assert_close(inp, out, None, o_ref, l_ref)
+
+
+# ------------------------------------------------------ short prefixes
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("d_qk", [192, 128])
+def test_fp8_cached_prefix_small(kernel, d_qk):
+    inp = make_inputs([7], [1100], 3, 3, d_qk, 128, "e4m3", seed=4)
+    out, lse = run_gpu(inp, flags=kernel)
+    o_ref, l_ref = reference(inp)
+    assert_close(inp, out, lse, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("mask", ["none", "causal", "window"])
+def test_varlen_edge_lengths(kernel, dtype, mask):
+    """Lengths (1, 0, 63, 64, 65, 128, 129, 700), GQA 8:2, d=128."""
+    inp = workload("edge", dtype=dtype, seed=5)
+    causal = mask == "causal"
+    wl = 128 if mask == "window" else -1
+    out, lse = run_gpu(inp, causal=causal, window_left=wl, flags=kernel)
+    o_ref, l_ref = reference(inp, 0.0, causal, wl)
+    assert_close(inp, out, lse, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("causal", [False, True])
+def test_different_q_and_k_lengths(kernel, causal):
+    """Bottom-right causal with Lq != Lk per sequence, including Lq > Lk rows
+    that see no key."""
+    lens_q, lens_k = [3, 17, 5, 40, 1], [200, 9, 5, 300, 0]
+    inp = make_inputs(lens_q, lens_k, 4, 2, 128, 128, "bf16", seed=6)
+    out, lse = run_gpu(inp, causal=causal, num_splits=3, flags=kernel)
+    o_ref, l_ref = reference(inp, 0.0, causal)
+    assert_close(inp, out, lse, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_zero_length_query_sequences_write_nothing(kernel):
+    lens_q, lens_k = [0, 2, 0, 1], [50, 60, 0, 70]
+    inp = make_inputs(lens_q, lens_k, 2, 2, 128, 128, "bf16", seed=7)
+    out, lse = run_gpu(inp, num_splits=2, flags=kernel, guard_rows=2)
+    o_ref, l_ref = reference(inp)
+    assert_close(inp, out, lse, o_ref, l_ref)
+    assert np.isnan(out[3:]).all() and np.isnan(lse[:, 3:]).all()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_custom_scale(kernel):
+    inp = workload("long_decode", kv=2000, h=2)
+    out, lse = run_gpu(inp, scale=0.31, num_splits=2, flags=kernel)
+    o_ref, l_ref = reference(inp, 0.31)
+    assert_close(inp, out, lse, o_ref, l_ref)
+
+
+# --------------------------------------------------- split ranges (exact)
+
+@pytest.mark.parametrize("causal,wl", [(False, -1), (True, -1), (True, 128), (False, 5)])
+def test_device_split_ranges_bit_exact(causal, wl):
+    lens_q = [1, 0, 63, 64, 65, 128, 129, 700, 3]
+    lens_k = [5000, 10, 63, 1000, 1, 128, 129, 700, 0]
+    cq = cu_seqlens(lens_q).cuda()
+    ck = cu_seqlens(lens_k).cuda()
+    for ns in (1, 3, 8, 128):
+        for tile_q in (1, 32, 128):
+            got = fa.fa_debug_split_ranges(cq, ck, max(lens_q), causal, wl, ns, tile_q).cpu()
+            for m in range(got.shape[0]):
+                for b, (lq, lk) in enumerate(zip(lens_q, lens_k)):
+                    i_lo = m * tile_q
+                    for s in range(ns):
+                        if i_lo >= lq:
+                            want = (0, 0)
+                        else:
+                            want = oracle.tile_split_key_range(
+                                i_lo, min(lq - 1, i_lo + tile_q - 1), lq, lk, causal, wl, ns, s)
+                        assert tuple(got[m, b, s].tolist()) == want, (m, b, s, ns, tile_q)
+
+
+# ---------------------------------------------------- graph replay, stages
+
+def test_cuda_graph_replay_matches_eager():
+    inp = workload("long_decode", kv=4000, h=4)
+    dev = torch.device("cuda:0")
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    cq, ck = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev)
+    out = torch.empty((1, 4, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((4, 1), dtype=torch.float32, device=dev)
+    nbytes = fa.fa_fwd_splitkv_workspace_size(1, 1, 4, 4, 128, 6)
+    ws = torch.empty(nbytes // 4, dtype=torch.float32, device=dev)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, 1, out, lse, ws, num_splits=6, stream=s)
+    s.synchronize()
+    eager = out.clone(), lse.clone()
+    out.zero_()
+    lse.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, 1, out, lse, ws, num_splits=6, stream=s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager[0]) and torch.equal(lse, eager[1])
+
+
+def test_partial_then_combine_equals_single_call():
+    inp = workload("long_decode", kv=3000, h=4)
+    a_out, a_lse = run_gpu(inp, num_splits=5)
+    dev = torch.device("cuda:0")
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    cq, ck = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev)
+    out = torch.empty((1, 4, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((4, 1), dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.fa_fwd_splitkv_workspace_size(1, 1, 4, 4, 128, 5) // 4,
+                     dtype=torch.float32, device=dev)
+    fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, 1, out, lse, ws, num_splits=5,
+                         flags=fa.FA_RUN_PARTIAL_ONLY)
+    fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, 1, out, lse, ws, num_splits=5,
+                         flags=fa.FA_RUN_COMBINE_ONLY)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.float().cpu().numpy(), a_out)
+    assert np.array_equal(lse.cpu().numpy(), a_lse)
+
+
+def test_bf16_shorthand_entry_point():
+    inp = workload("long_decode", kv=2500, h=2)
+    dev = torch.device("cuda:0")
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    cq, ck = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev)
+    out = torch.empty((1, 2, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((2, 1), dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.fa_fwd_splitkv_workspace_size(1, 1, 2, 2, 128, 4) // 4,
+                     dtype=torch.float32, device=dev)
+    fa.fa_fwd_splitkv(q, k, v, cq, ck, 1, out, lse, ws, num_splits=4)
+    torch.cuda.synchronize()
+    o_ref, l_ref = reference(inp)
+    assert_close(inp, out.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref)
+
+
+def test_inconsistent_cu_seqlens_reported_on_device():
+    """A sequence longer than max_seqlen_q is skipped and flagged, never
+    written out of range."""
+    inp = make_inputs([3], [100], 2, 2, 128, 128, "bf16", seed=8)
+    dev = torch.device("cuda:0")
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    cq, ck = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev)
+    out = torch.full((3, 2, 128), float("nan"), dtype=torch.bfloat16, device=dev)
+    fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, 2, out, None, None, num_splits=1)  # max_seqlen_q=2 < 3
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_error(clear=True) == -6
+    assert torch.isnan(out).all()
+    assert fa.fa_get_device_error() == 0
+
+
+# ------------------------------------------ full-size workloads (sampled)
+
+def test_full_long_decode_sampled_heads():
+    """B=1, Q=1, K=131072, H=32, D=128, automatic splits (the benchmark's
+    launch configuration), 4 of 32 heads checked against the oracle."""
+    inp = workload("long_decode", device="cuda")
+    out, lse = run_gpu(inp)
+    heads = [0, 7, 19, 31]
+    o_ref, l_ref = reference(inp, heads=heads)
+    assert_close(inp, out, lse, o_ref, l_ref, heads=heads)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
+def test_full_gqa_decode_varlen():
+    inp = workload("gqa_decode", device="cuda")
+    assert sum(gqa_decode_lengths(0)) == int(inp.cu_seqlens_k[-1])
+    out, lse = run_gpu(inp)
+    heads = [0, 5, 14, 31]
+    o_ref, l_ref = reference(inp, heads=heads)
+    assert_close(inp, out, lse, o_ref, l_ref, heads=heads)
+
+
+@pytest.mark.parametrize("kv", [11008, 16384])
+def test_full_fp8_cached_prefix(kv):
+    inp = workload("fp8_prefix", kv=kv, device="cuda")
+    out, lse = run_gpu(inp)
+    o_ref, l_ref = reference(inp)
+    assert_close(inp, out, lse, o_ref, l_ref)

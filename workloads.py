@@ -5,9 +5,11 @@ and the CUDA side (tests, bench): it only draws random numbers and packs
 them.  It holds none of the attention arithmetic.
 
 Recipe (same for every workload):
-* torch.Generator on the CPU, manual_seed(seed), drawing Q, then K, then V
-  as float32 N(0, 1), in chunks of CHUNK elements, each chunk cast to the
-  storage dtype.
+* torch.Generator on the CPU (or, for the large workloads the GPU tests and
+  the benchmark use, on the CUDA device: same recipe, the device's Philox
+  generator), manual_seed(seed), drawing Q, then K, then V as float32
+  N(0, 1), in chunks of CHUNK elements, each chunk cast to the storage dtype.
+  Both sides always see the same tensor: the oracle gets a host copy of it.
 * Packed varlen layout: Q [total_q, h_q, d_qk], K [total_k, h_kv, d_qk],
   V [total_k, h_kv, d_v], cu_seqlens int32 [B+1] exclusive prefix sums.
 * FP8 e4m3: the float32 draw x of a whole tensor gives descale = amax/448 and
@@ -66,10 +68,12 @@ def _randn_chunked(gen: torch.Generator, shape, out_dtype) -> torch.Tensor:
     n = 1
     for s in shape:
         n *= int(s)
-    out = torch.empty(n, dtype=out_dtype)
+    dev = gen.device
+    out = torch.empty(n, dtype=out_dtype, device=dev)
     for s0 in range(0, n, CHUNK):
         s1 = min(n, s0 + CHUNK)
-        out[s0:s1] = torch.randn(s1 - s0, generator=gen, dtype=torch.float32).to(out_dtype)
+        out[s0:s1] = torch.randn(s1 - s0, generator=gen, dtype=torch.float32,
+                                 device=dev).to(out_dtype)
     return out.view(*shape)
 
 
@@ -89,10 +93,11 @@ def cu_seqlens(lengths) -> torch.Tensor:
 
 
 def make_inputs(lens_q, lens_k, h_q: int, h_kv: int, d_qk: int, d_v: int,
-                dtype: str = "bf16", seed: int = 0) -> Inputs:
+                dtype: str = "bf16", seed: int = 0, device: str = "cpu") -> Inputs:
+    """Q/K/V on `device` (cu_seqlens always on the host)."""
     assert len(lens_q) == len(lens_k)
     total_q, total_k = int(sum(lens_q)), int(sum(lens_k))
-    gen = torch.Generator().manual_seed(seed)
+    gen = torch.Generator(device=device).manual_seed(seed)
     if dtype == "e4m3":
         q, dq = _randn_e4m3(gen, (total_q, h_q, d_qk))
         k, dk = _randn_e4m3(gen, (total_k, h_kv, d_qk))
@@ -123,29 +128,29 @@ PREFILL_LENGTHS = (4096, 512, 3072, 1024, 2560, 1536, 2048, 1536)
 EDGE_LENGTHS = (1, 0, 63, 64, 65, 128, 129, 700)
 
 
-def workload(name: str, seed: int = 0, **kw) -> Inputs:
+def workload(name: str, seed: int = 0, device: str = "cpu", **kw) -> Inputs:
     """The named workloads; keyword overrides resize them for tests."""
     if name == "tiny_decode":
         kv = kw.get("kv", 1024)
-        return make_inputs([1], [kv], 4, 4, 64, 64, "bf16", seed)
+        return make_inputs([1], [kv], 4, 4, 64, 64, "bf16", seed, device)
     if name == "long_decode":
         kv = kw.get("kv", 131072)
         h = kw.get("h", 32)
-        return make_inputs([1], [kv], h, h, 128, 128, "bf16", seed)
+        return make_inputs([1], [kv], h, h, 128, 128, "bf16", seed, device)
     if name == "gqa_decode":
         batch = kw.get("batch", 32)
         lens_k = kw.get("lens_k") or gqa_decode_lengths(seed, batch)
-        return make_inputs([1] * len(lens_k), lens_k, 32, 8, 128, 128, "bf16", seed)
+        return make_inputs([1] * len(lens_k), lens_k, 32, 8, 128, 128, "bf16", seed, device)
     if name == "fp8_prefix":
         kv = kw.get("kv", 16384)
         q = kw.get("q", 70)
         h = kw.get("h", 12)
-        return make_inputs([q], [kv], h, h, 192, 128, "e4m3", seed)
+        return make_inputs([q], [kv], h, h, 192, 128, "e4m3", seed, device)
     if name == "prefill":
         lens = kw.get("lens", PREFILL_LENGTHS)
         return make_inputs(lens, lens, 16, kw.get("h_kv", 16), 128, 128,
-                           kw.get("dtype", "bf16"), seed)
+                           kw.get("dtype", "bf16"), seed, device)
     if name == "edge":
         lens = kw.get("lens", EDGE_LENGTHS)
-        return make_inputs(lens, lens, 8, 2, 128, 128, kw.get("dtype", "bf16"), seed)
+        return make_inputs(lens, lens, 8, 2, 128, 128, kw.get("dtype", "bf16"), seed, device)
     raise KeyError(name)

@@ -54,6 +54,11 @@ struct SimtCfg {
   static_assert(DV % 32 == 0, "d_v must be a multiple of 32");
   static_assert(BPL == 2 || BPL == 4 || BPL == 8 || BPL == 16, "unsupported V lane width");
   static_assert(RT <= NW, "one epilogue warp per row");
+  // Chunk c uses stage c % NS and warp c % NW.  With NS a multiple of NW the
+  // previous user of a stage (chunk c - NS) is the same warp, which has
+  // already consumed it, so a parity wait can never match a phase two behind
+  // (a different warp could still be waiting on that older load).
+  static_assert(NS % NW == 0 && NS >= 2 * NW, "stages must be a multiple of the consumer warps");
   static_assert(NPV <= 2 && NPK <= 4, "head dim too large for this kernel");
 };
 

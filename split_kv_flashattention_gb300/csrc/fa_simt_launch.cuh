@@ -8,19 +8,22 @@
 
 namespace fa {
 
-// Stage ring sized so two CTAs fit on one SM (about 100 KB each).
-template <int DT, int DQK, int DV>
+// Stage ring: about 96 KB (two CTAs per SM) but at least two stages per
+// consumer warp, and a multiple of the consumer warps.
+template <int DT, int DQK, int DV, int NW>
 struct SimtStages {
   static constexpr int ES = Elem<DT>::size;
   static constexpr int STAGE = (((DQK * ES + 127) / 128) + ((DV * ES + 127) / 128)) * 4096;
-  static constexpr int NS = (96 * 1024) / STAGE > 12 ? 12 : (96 * 1024) / STAGE;
+  static constexpr int BUDGET = (96 * 1024) > 2 * NW * STAGE ? (96 * 1024) : 2 * NW * STAGE;
+  static constexpr int NS_RAW = BUDGET / STAGE > 16 ? 16 : BUDGET / STAGE;
+  static constexpr int NS = NS_RAW - NS_RAW % NW;
 };
 
 template <int DT, int DQK, int DV, int RT>
 cudaError_t launch_simt_one(const FwdParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                             dim3 grid, cudaStream_t stream) {
   constexpr int NW = 4;
-  constexpr int NS = SimtStages<DT, DQK, DV>::NS;
+  constexpr int NS = SimtStages<DT, DQK, DV, NW>::NS;
   using C = SimtCfg<DT, DQK, DV, RT, NW, NS>;
   auto kern = simt_splitkv_kernel<DT, DQK, DV, RT, NW, NS>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM);

@@ -137,6 +137,38 @@ FA_API int fa_fwd_splitkv(const void* q, const void* k, const void* v, const int
                    int causal, int window_left, int num_splits, void* out, float* lse,
                    void* workspace, void* stream);
 
+/*
+ * fa_fwd_splitkv_noalloc -- the same forward pass for callers that cannot
+ * allocate device memory (no counterpart on the pages this library follows;
+ * it is an addition for embedding).  Examples: code running under a runtime
+ * or framework that owns all device allocations and gives the call site no
+ * allocator, plugins without an allocator handle, and latency-critical paths
+ * where cudaMalloc (which synchronises the device) is not allowed.  The
+ * caller still passes inputs and outputs; the fp32 split workspace comes
+ * from a fixed array of FA_NOALLOC_SCRATCH_BYTES in device global memory
+ * defined by the library, which every device that loads it (at the latest on
+ * the first call there) keeps until the process exits.
+ *
+ * Arguments are those of fa_fwd_splitkv_ex without workspace and
+ * workspace_bytes.  The call allocates nothing and frees nothing.  Problems
+ * whose workspace (fa_fwd_splitkv_workspace_size) exceeds
+ * FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_WORKSPACE before any
+ * launch.  The first call on each device looks up the array's device address
+ * with that device current (make it before any stream capture).  All calls
+ * on a device share the one array: calls that may overlap on the GPU (other
+ * streams, other host threads) race on it and must be serialised by the
+ * caller.  The array keeps the last call's contents; nothing in it needs
+ * clearing because every partial a call reads was written by that call.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20) /* 8 MiB */
+FA_API int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v,
+                                  const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                                  int total_q, int total_k, int max_seqlen_q, int h_q, int h_kv,
+                                  int d_qk, int d_v, float scale, int causal, int window_left,
+                                  int num_splits, void* out, float* lse, int in_dtype,
+                                  int out_dtype, const float* descale_q, const float* descale_k,
+                                  const float* descale_v, int flags, void* stream);
+
 /* Bytes of workspace fa_fwd_splitkv_ex needs for these sizes: the fp32
  * partial outputs [ns, batch*max_seqlen_q, h_q, d_v] followed by the partial
  * LSEs [ns, batch*max_seqlen_q, h_q]; 0 when the resolved split count is 1.

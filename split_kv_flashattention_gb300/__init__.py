@@ -22,7 +22,7 @@ __all__ = [
     "fa_fwd_splitkv_workspace_size", "fa_plan", "fa_debug_split_ranges",
     "fa_get_device_error", "fa_status_string", "fa_version", "forward",
     "FA_KERNEL_AUTO", "FA_KERNEL_SIMT", "FA_KERNEL_UMMA", "FA_RUN_PARTIAL_ONLY",
-    "FA_RUN_COMBINE_ONLY", "DTYPE_CODES",
+    "FA_RUN_COMBINE_ONLY", "DTYPE_CODES", "fa_fwd_splitkv_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libfa_splitkv.so")
@@ -33,7 +33,9 @@ DTYPE_CODES = {torch.bfloat16: 0, torch.float16: 1, torch.float8_e4m3fn: 2}
 EXPORTED = (
     "fa_fwd_splitkv_ex", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_plan",
     "fa_debug_split_ranges", "fa_get_device_error", "fa_status_string", "fa_version",
+    "fa_fwd_splitkv_noalloc",
 )
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class FaError(RuntimeError):
@@ -69,6 +71,10 @@ def library() -> ctypes.CDLL:
     lib.fa_fwd_splitkv.argtypes = [
         _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
         _c_float, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp]
+    lib.fa_fwd_splitkv_noalloc.restype = _c_int
+    lib.fa_fwd_splitkv_noalloc.argtypes = [
+        _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+        _c_float, _c_int, _c_int, _c_int, _vp, _vp, _c_int, _c_int, _vp, _vp, _vp, _c_int, _vp]
     lib.fa_fwd_splitkv_workspace_size.restype = _c_size
     lib.fa_fwd_splitkv_workspace_size.argtypes = [_c_int] * 6
     lib.fa_plan.restype = _c_int
@@ -160,6 +166,27 @@ def fa_fwd_splitkv_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, ou
         DTYPE_CODES[out.dtype], _ptr(descale_q), _ptr(descale_k), _ptr(descale_v), int(flags),
         _stream(stream))
     _check(st, "fa_fwd_splitkv_ex")
+
+
+def fa_fwd_splitkv_noalloc(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, out,
+                           lse=None, scale: float = 0.0, causal: bool = False,
+                           window_left: int = -1, num_splits: int = 0, descale_q=None,
+                           descale_k=None, descale_v=None, flags: int = FA_KERNEL_AUTO,
+                           stream=None):
+    """Calls fa_fwd_splitkv_noalloc: the forward pass without a caller
+    workspace, for callers that cannot allocate device memory.  The split
+    workspace is the library's fixed device array of NOALLOC_SCRATCH_BYTES;
+    larger problems raise FaError(FA_ERR_WORKSPACE).  Calls that overlap on
+    the GPU share that array and must be serialised by the caller."""
+    total_q, h_q, d_qk = q.shape
+    total_k, h_kv, _ = k.shape
+    st = library().fa_fwd_splitkv_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+        cu_seqlens_q.numel() - 1, total_q, total_k, max_seqlen_q, h_q, h_kv, d_qk, v.shape[2],
+        float(scale), int(causal), int(window_left), int(num_splits), _ptr(out), _ptr(lse),
+        DTYPE_CODES[q.dtype], DTYPE_CODES[out.dtype], _ptr(descale_q), _ptr(descale_k),
+        _ptr(descale_v), int(flags), _stream(stream))
+    _check(st, "fa_fwd_splitkv_noalloc")
 
 
 def fa_fwd_splitkv(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, out, lse=None,

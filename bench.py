@@ -53,7 +53,80 @@ WORKLOADS = {
                        desc="short cached-prefix FP8: B=1, Q=70, H=12, D_qk=192, D_v=128, KV=16384, e4m3"),
     "fp8_prefix_11k": dict(name="fp8_prefix", kw={"kv": 11008},
                            desc="short cached-prefix FP8: B=1, Q=70, H=12, D_qk=192, D_v=128, KV=11008, e4m3"),
+    "prefill": dict(name="prefill", kw={"h_kv": 16}, causal=False, kind="tensor",
+                    desc="varlen prefill: 16384 tokens (4096,512,3072,1024,2560,1536,2048,1536), "
+                         "H_q=H_kv=16, D=128, bf16, no mask"),
+    "prefill_causal": dict(name="prefill", kw={"h_kv": 16}, causal=True, kind="tensor",
+                           desc="varlen prefill: 16384 tokens (4096,512,3072,1024,2560,1536,2048,1536), "
+                                "H_q=H_kv=16, D=128, bf16, causal"),
+    "prefill_gqa": dict(name="prefill", kw={"h_kv": 4}, causal=False, kind="tensor",
+                        desc="varlen prefill: 16384 tokens, H_q=16, H_kv=4, D=128, bf16, no mask"),
+    "prefill_gqa_causal": dict(name="prefill", kw={"h_kv": 4}, causal=True, kind="tensor",
+                               desc="varlen prefill: 16384 tokens, H_q=16, H_kv=4, D=128, bf16, causal"),
 }
+
+
+def attended_pairs(inp, causal):
+    """(query, key) pairs the mask allows, summed over sequences (the FLOP
+    count of the cutlass varlen page: attended pairs only)."""
+    cq = inp.cu_seqlens_q.tolist()
+    ck = inp.cu_seqlens_k.tolist()
+    total = 0
+    for b in range(len(cq) - 1):
+        lq, lk = cq[b + 1] - cq[b], ck[b + 1] - ck[b]
+        if not causal:
+            total += lq * lk
+        else:
+            for i in range(lq):
+                total += max(0, min(lk, i + lk - lq + 1))
+    return total
+
+
+def flops(inp, causal):
+    return 2 * (inp.d_qk + inp.d_v) * inp.h_q * attended_pairs(inp, causal)
+
+
+def measured_tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0) or 0), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+def prefill_secondary(fa, dev, steps, warmup):
+    """Varlen prefill TFLOPS (the metric's second part) for no-mask and causal."""
+    res = {}
+    peak, _, src = measured_tensor_peak()
+    for name in ("prefill", "prefill_causal"):
+        spec = WORKLOADS[name]
+        inp = workload(spec["name"], device=str(dev), **spec["kw"])
+        causal = spec["causal"]
+        out = torch.empty((inp.q.shape[0], inp.h_q, inp.d_v), dtype=inp.q.dtype, device=dev)
+        lse = torch.empty((inp.h_q, inp.q.shape[0]), dtype=torch.float32, device=dev)
+        cq, ck = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev)
+        stream = torch.cuda.current_stream(dev)
+
+        def step():
+            fa.fa_fwd_splitkv_ex(inp.q, inp.k, inp.v, cq, ck, inp.max_seqlen_q, out, lse, None,
+                                 0.0, causal, -1, 0, None, None, None, 0, stream)
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / steps
+        tf = flops(inp, causal) / (ms * 1e-3) / 1e12
+        res[name] = {"ms": ms, "tflops": tf, "frac": tf / peak, "flops": flops(inp, causal)}
+    res["peak_tflops"] = peak
+    res["peak_source"] = src + " bf16 dense (burst)"
+    res["workload"] = WORKLOADS["prefill"]["desc"].replace(", no mask", "")
+    return res
 
 
 def parse():
@@ -66,7 +139,10 @@ def parse():
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "umma"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the varlen prefill TFLOPS measurement of the default line")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--kv", type=int, default=0, help="override the key length (long_decode)")
     return ap.parse_args()
 
 
@@ -96,12 +172,21 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {
+    "simt_splitkv": ("fa_simt.cuh", "fa_simt_launch.cuh", "fa_simt_bf16.cu", "fa_common.cuh",
+                     "fa_ptx.cuh", "fa_convert.cuh"),
+    "umma_splitkv": ("fa_umma.cuh", "fa_umma_launch.cuh", "fa_umma_bf16.cu", "fa_umma_e4m3.cu",
+                     "fa_common.cuh", "fa_ptx.cuh", "fa_convert.cuh"),
+}
+
+
+def kernel_source_hash(kernel_tag):
+    """Hash of the sources a kernel is built from (its ncu counters are only
+    valid for these exact sources)."""
     h = hashlib.sha256()
-    for f in sorted(os.listdir(CSRC)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(CSRC, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    for f in KERNEL_SOURCES[kernel_tag]:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
@@ -114,7 +199,7 @@ def profiled_traffic(kernel_tag, workload_name):
     text = open(path).read()
     m_hash = re.search(r"^source_hash:\s*(\S+)", text, re.M)
     m_t = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
-    if not m_hash or not m_t or m_hash.group(1) != kernel_source_hash():
+    if not m_hash or not m_t or m_hash.group(1) != kernel_source_hash(kernel_tag):
         return None
     return float(m_t.group(1))
 
@@ -177,9 +262,9 @@ class ClockSampler:
                 "samples": len(inside)}
 
 
-def cpu_baseline(inp_cpu, budget_s=12.0, heads=2):
+def cpu_baseline(inp_cpu, budget_s=12.0, heads=2, causal=False, kind="hbm"):
     """The float64 oracle on `heads` query heads of the workload, repeated for
-    about budget_s seconds on the host cores."""
+    about budget_s seconds on the host cores; reported in the metric's unit."""
     import oracle
 
     group = inp_cpu.h_q // inp_cpu.h_kv
@@ -190,17 +275,22 @@ def cpu_baseline(inp_cpu, budget_s=12.0, heads=2):
     v = inp_cpu.v[:, kvs]
     es = 1 if inp_cpu.dtype == "e4m3" else 2
     tq, tk = q.shape[0], k.shape[0]
-    sample_bytes = (tk * len(kvs) * (inp_cpu.d_qk + inp_cpu.d_v) * es
-                    + tq * heads * (inp_cpu.d_qk * es + inp_cpu.d_v * 2))
+    if kind == "tensor":
+        sample_work = 2 * (inp_cpu.d_qk + inp_cpu.d_v) * heads * attended_pairs(inp_cpu, causal)
+        unit = "TFLOPS"
+    else:
+        sample_work = (tk * len(kvs) * (inp_cpu.d_qk + inp_cpu.d_v) * es
+                       + tq * heads * (inp_cpu.d_qk * es + inp_cpu.d_v * 2))
+        unit = "TB/s"
     reps, t_total = 0, 0.0
     while t_total < budget_s or reps == 0:
         t = time.perf_counter()
         oracle.attention_forward(q, k, v, inp_cpu.cu_seqlens_q, inp_cpu.cu_seqlens_k,
-                                 heads, len(kvs), 0.0, False, -1, inp_cpu.descale_q,
+                                 heads, len(kvs), 0.0, causal, -1, inp_cpu.descale_q,
                                  inp_cpu.descale_k, inp_cpu.descale_v)
         t_total += time.perf_counter() - t
         reps += 1
-    return {"value": sample_bytes * reps / t_total / 1e12, "unit": "TB/s",
+    return {"value": sample_work * reps / t_total / 1e12, "unit": unit,
             "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{heads} of {inp_cpu.h_q} query heads (all keys), float64 oracle, "
                       f"{reps} repetitions in {t_total:.1f} s, numpy/BLAS default threads",
@@ -213,27 +303,34 @@ def inp_host(inp):
 
 
 def run_reference(args, spec, rank):
+    """The oracle as the reference arm: one oracle call on a bounded sample
+    (one query head, all keys) per step, on the host cores."""
     if rank != 0:
         return
-    inp = workload(spec["name"], **spec["kw"])
-    steps_t = []
+    kind = spec.get("kind", "hbm")
+    causal = spec.get("causal", False)
+    kw = dict(spec["kw"])
+    if args.kv:
+        kw["kv"] = args.kv
+    inp = workload(spec["name"], **kw)
+    vals = []
     cb = None
     for i in range(args.warmup + args.steps):
-        r = cpu_baseline(inp, budget_s=0.0, heads=1)
+        cb = cpu_baseline(inp, budget_s=0.0, heads=1, causal=causal, kind=kind)
         if i >= args.warmup:
-            steps_t.append(r)
-        cb = r
-    vals = [r["value"] for r in steps_t] or [cb["value"]]
-    value = statistics.median(vals)
+            vals.append(cb["value"])
+    value = statistics.median(vals) if vals else cb["value"]
+    unit = cb["unit"]
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TB/s",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": spec["desc"]},
-        "cpu_baseline": {"value": value, "unit": "TB/s", "cores": os.cpu_count(),
-                         "kind": "oracle", "sample": cb["sample"].split(",")[0] +
-                         ", one oracle call per step"},
-        "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0,
+        "cpu_baseline": {"value": value, "unit": unit, "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": "1 of %d query heads (all keys), one float64 oracle call per step"
+                                   % inp.h_q},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -241,6 +338,8 @@ def run_reference(args, spec, rank):
 def main():
     args = parse()
     spec = WORKLOADS[args.workload]
+    kind = spec.get("kind", "hbm")
+    causal = spec.get("causal", False)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
@@ -259,7 +358,10 @@ def main():
 
     kernel_flag = {"auto": fa.FA_KERNEL_AUTO, "simt": fa.FA_KERNEL_SIMT,
                    "umma": fa.FA_KERNEL_UMMA}[args.kernel]
-    inp = workload(spec["name"], device=str(dev), **spec["kw"])
+    kw = dict(spec["kw"])
+    if args.kv:
+        kw["kv"] = args.kv
+    inp = workload(spec["name"], device=str(dev), **kw)
     q, k, v = inp.q, inp.k, inp.v
     cq, ck = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev)
     out_dtype = torch.bfloat16 if inp.dtype == "e4m3" else q.dtype
@@ -275,17 +377,21 @@ def main():
         dk = torch.tensor([inp.descale_k], dtype=torch.float32, device=dev)
         dv = torch.tensor([inp.descale_v], dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    rows = inp.max_seqlen_q * (inp.h_q // inp.h_kv)
+    uses_umma = args.kernel == "umma" or (args.kernel == "auto" and rows > (2 if (
+        inp.dtype == "e4m3" and inp.d_qk == 192) else 4))
+    kern_tag = "umma_splitkv" if uses_umma else "simt_splitkv"
+
+    def call(flags):
+        fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, inp.max_seqlen_q, out, lse, ws, 0.0, causal, -1,
+                             args.num_splits, dq, dk, dv, flags, stream)
 
     def partial():
-        fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, inp.max_seqlen_q, out, lse, ws, 0.0, False, -1,
-                             args.num_splits, dq, dk, dv, kernel_flag | fa.FA_RUN_PARTIAL_ONLY,
-                             stream)
+        call(kernel_flag | fa.FA_RUN_PARTIAL_ONLY)
 
     def combine():
         if ns > 1:
-            fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, inp.max_seqlen_q, out, lse, ws, 0.0, False, -1,
-                                 args.num_splits, dq, dk, dv,
-                                 kernel_flag | fa.FA_RUN_COMBINE_ONLY, stream)
+            call(kernel_flag | fa.FA_RUN_COMBINE_ONLY)
 
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -325,7 +431,13 @@ def main():
     total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
     metric_bytes, partial_bytes = byte_counts(inp, ns)
-    value = world * metric_bytes / (ms_per_step * 1e-3) / 1e12
+    work_flops = flops(inp, causal)
+    if kind == "tensor":
+        unit = "TFLOPS"
+        value = world * work_flops / (ms_per_step * 1e-3) / 1e12
+    else:
+        unit = "TB/s"
+        value = world * metric_bytes / (ms_per_step * 1e-3) / 1e12
 
     # ---- end to end through the public call with host buffers
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
@@ -342,8 +454,7 @@ def main():
         v.copy_(hv, non_blocking=True)
         cq.copy_(hcq, non_blocking=True)
         ck.copy_(hck, non_blocking=True)
-        fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, inp.max_seqlen_q, out, lse, ws, 0.0, False, -1,
-                             args.num_splits, dq, dk, dv, kernel_flag, stream)
+        call(kernel_flag)
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
 
@@ -360,35 +471,51 @@ def main():
     te = torch.tensor([e0.elapsed_time(e1) / e2e_steps], dtype=torch.float64, device=dev)
     if world > 1:
         torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
-    e2e_value = world * metric_bytes / (float(te.item()) * 1e-3) / 1e12
+    e2e_ms = float(te.item())
+    e2e_value = world * (work_flops if kind == "tensor" else metric_bytes) / (e2e_ms * 1e-3) / 1e12
+
+    secondary = None
+    if kind == "hbm" and world == 1 and not args.no_prefill:
+        secondary = prefill_secondary(fa, dev, steps=max(3, min(args.steps, 30)),
+                                      warmup=max(3, min(args.warmup, 5)))
 
     if rank == 0:
-        peak_gbs, peak_src = measured_peaks()
-        achieved_gbs = partial_bytes / (partial_ms * 1e-3) / 1e9
-        kern_tag = "simt_splitkv" if args.kernel in ("auto", "simt") else "umma_splitkv"
-        traffic = profiled_traffic(kern_tag, args.workload)
+        if kind == "tensor":
+            peak, peak_sus, src = measured_tensor_peak()
+            achieved = work_flops / (partial_ms * 1e-3) / 1e12
+            roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "peak_source": src + " bf16 dense (burst)",
+                    "traffic": profiled_traffic(kern_tag, args.workload),
+                    "kernel": f"{kern_tag} partial kernel", "partial_ms": partial_ms,
+                    "algorithmic_flops_per_launch": work_flops}
+        else:
+            peak_gbs, peak_src = measured_peaks()
+            achieved_gbs = partial_bytes / (partial_ms * 1e-3) / 1e9
+            roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": peak_gbs, "unit": "GB/s",
+                    "frac": achieved_gbs / peak_gbs, "peak_source": peak_src,
+                    "traffic": profiled_traffic(kern_tag, args.workload),
+                    "kernel": f"{kern_tag} partial kernel", "partial_ms": partial_ms,
+                    "algorithmic_bytes_per_launch": partial_bytes}
         line = {
-            "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world,
+            "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if inp.dtype == "bf16" else inp.dtype, "data": "synthetic",
             "config": {"workload": spec["desc"], "num_splits": ns,
-                       "num_splits_requested": args.num_splits, "kernel": args.kernel,
-                       "l2": "inputs larger than L2 (K+V %.2f GB)" % (
-                           (inp.k.numel() + inp.v.numel()) * inp.k.element_size() / 1e9),
+                       "num_splits_requested": args.num_splits, "kernel": kern_tag,
+                       "l2": "inputs larger than L2 (Q+K+V %.2f GB)" % (
+                           sum(x.numel() * x.element_size() for x in (q, k, v)) / 1e9),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak_gbs,
-                         "unit": "GB/s", "frac": achieved_gbs / peak_gbs,
-                         "peak_source": peak_src, "traffic": traffic,
-                         "kernel": "split partial kernel", "partial_ms": partial_ms,
-                         "algorithmic_bytes_per_launch": partial_bytes},
-            "e2e": {"value": e2e_value, "unit": "TB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "roofline": roof,
+            "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_ms},
             "gpu_launches": args.steps * (2 if ns > 1 else 1),
             "clocks": clocks,
         }
+        if secondary is not None:
+            line["prefill"] = secondary
         if not args.no_cpu_baseline and world == 1:
-            line["cpu_baseline"] = cpu_baseline(inp_host(inp))
+            line["cpu_baseline"] = cpu_baseline(inp_host(inp), causal=causal, kind=kind)
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -79,10 +79,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 }
 
 // 3-D map over a packed [rows, heads, dim] buffer with a 128-byte-wide,
-// 128B-swizzled box of box_rows rows of one head.  Rows past `rows` and
-// columns past `dim` read as zero.
+// 128B-swizzled box of box_heads heads x box_rows rows.  Rows past `rows`
+// and columns past `dim` read as zero.
 int make_tmap_3d(CUtensorMap* m, const void* base, int dtype, int dim, int heads, int rows,
-                 int box_rows) {
+                 int box_rows, int box_heads = 1) {
   auto enc = encoder();
   if (enc == nullptr) return FA_ERR_CUDA;
   const int es = dtype == kE4M3 ? 1 : 2;
@@ -91,7 +91,7 @@ int make_tmap_3d(CUtensorMap* m, const void* base, int dtype, int dim, int heads
                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   cuuint64_t gdim[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
   cuuint64_t gstride[2] = {(cuuint64_t)dim * es, (cuuint64_t)dim * es * heads};
-  cuuint32_t box[3] = {(cuuint32_t)(128 / es), 1u, (cuuint32_t)box_rows};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / es), (cuuint32_t)box_heads, (cuuint32_t)box_rows};
   cuuint32_t estride[3] = {1u, 1u, 1u};
   CUresult r = enc(m, t, 3, const_cast<void*>(base), gdim, gstride, box, estride,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -167,6 +167,17 @@ cudaError_t launch_simt(int dtype, int d_qk, int d_v, int rt, const FwdParams& p
     case kBF16: return launch_simt_bf16(d_qk, d_v, rt, p, tmK, tmV, grid, stream);
     case kFP16: return launch_simt_fp16(d_qk, d_v, rt, p, tmK, tmV, grid, stream);
     case kE4M3: return launch_simt_e4m3(d_qk, d_v, rt, p, tmK, tmV, grid, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_umma(int dtype, int d_qk, int d_v, const FwdParams& p, const CUtensorMap& tmQ,
+                        const CUtensorMap& tmK, const CUtensorMap& tmV, dim3 grid,
+                        cudaStream_t stream) {
+  switch (dtype) {
+    case kBF16: return launch_umma_bf16(d_qk, d_v, p, tmQ, tmK, tmV, grid, stream);
+    case kFP16: return launch_umma_fp16(d_qk, d_v, p, tmQ, tmK, tmV, grid, stream);
+    case kE4M3: return launch_umma_e4m3(d_qk, d_v, p, tmQ, tmK, tmV, grid, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -300,7 +311,6 @@ int fa_fwd_splitkv_ex(const void* q, const void* k, const void* v, const int* cu
       ((long long)h_kv * d_v * es) % 16)
     return FA_ERR_INVALID_ARG;
   if (in_dtype == kE4M3 && (!descale_q || !descale_k || !descale_v)) return FA_ERR_INVALID_ARG;
-  if (kernel_sel == FA_KERNEL_UMMA) return FA_ERR_UNSUPPORTED;
 
   // ---- plan (the device is queried only for an automatic split count)
   int sms = 1;
@@ -355,21 +365,36 @@ int fa_fwd_splitkv_ex(const void* q, const void* k, const void* v, const int* cu
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  // ---- CUDA-core streaming kernel
+  // ---- kernel choice: few rows per KV head (decode) stream on the CUDA
+  // cores; more rows form a dense contraction for the tensor cores.
   const int rows = max_seqlen_q * p.group;
   const int rt_max = simt_max_rows(in_dtype, d_qk, d_v);
-  int rt = 1;
-  while (rt < rows && rt < rt_max) rt *= 2;
-  p.tile_rows = rt;
-  CUtensorMap tmK, tmV;
-  st = make_tmap_3d(&tmK, k, in_dtype, d_qk, h_kv, total_k, 32);
-  if (st != FA_OK) return st;
-  st = make_tmap_3d(&tmV, v, in_dtype, d_v, h_kv, total_k, 32);
-  if (st != FA_OK) return st;
-  dim3 grid((unsigned)ceil_div(rows, rt), (unsigned)(batch * h_kv), (unsigned)ns);
-  if (grid.x > 0x7fffffffu || grid.y > 65535u) return FA_ERR_INVALID_ARG;
+  const bool use_umma =
+      kernel_sel == FA_KERNEL_UMMA || (kernel_sel == FA_KERNEL_AUTO && rows > rt_max);
+  if ((unsigned)(batch * h_kv) > 65535u) return FA_ERR_UNSUPPORTED;
   if (run_partial) {
-    cudaError_t e = launch_simt(in_dtype, d_qk, d_v, rt, p, tmK, tmV, grid, s);
+    CUtensorMap tmK, tmV;
+    const int box_keys = use_umma ? kBlockN : 32;
+    st = make_tmap_3d(&tmK, k, in_dtype, d_qk, h_kv, total_k, box_keys);
+    if (st != FA_OK) return st;
+    st = make_tmap_3d(&tmV, v, in_dtype, d_v, h_kv, total_k, box_keys);
+    if (st != FA_OK) return st;
+    cudaError_t e;
+    if (use_umma) {
+      const int qpt = 128 / p.group;
+      p.tile_rows = qpt * p.group;
+      CUtensorMap tmQ;
+      st = make_tmap_3d(&tmQ, q, in_dtype, d_qk, h_q, total_q, qpt, p.group);
+      if (st != FA_OK) return st;
+      dim3 grid((unsigned)ceil_div(max_seqlen_q, qpt), (unsigned)(batch * h_kv), (unsigned)ns);
+      e = launch_umma(in_dtype, d_qk, d_v, p, tmQ, tmK, tmV, grid, s);
+    } else {
+      int rt = 1;
+      while (rt < rows && rt < rt_max) rt *= 2;
+      p.tile_rows = rt;
+      dim3 grid((unsigned)ceil_div(rows, rt), (unsigned)(batch * h_kv), (unsigned)ns);
+      e = launch_simt(in_dtype, d_qk, d_v, rt, p, tmK, tmV, grid, s);
+    }
     if (e != cudaSuccess) return FA_ERR_CUDA;
   }
   if (run_combine && ns > 1) {

@@ -24,6 +24,20 @@ cudaError_t launch_simt_fp16(int d_qk, int d_v, int rt, const FwdParams& p, cons
 cudaError_t launch_simt_e4m3(int d_qk, int d_v, int rt, const FwdParams& p, const CUtensorMap& tmK,
                              const CUtensorMap& tmV, dim3 grid, cudaStream_t stream);
 
+// Launch the tcgen05 split kernel.  grid = (query tiles, batch*h_kv, ns).
+cudaError_t launch_umma(int dtype, int d_qk, int d_v, const FwdParams& p, const CUtensorMap& tmQ,
+                        const CUtensorMap& tmK, const CUtensorMap& tmV, dim3 grid,
+                        cudaStream_t stream);
+cudaError_t launch_umma_bf16(int d_qk, int d_v, const FwdParams& p, const CUtensorMap& tmQ,
+                             const CUtensorMap& tmK, const CUtensorMap& tmV, dim3 grid,
+                             cudaStream_t stream);
+cudaError_t launch_umma_fp16(int d_qk, int d_v, const FwdParams& p, const CUtensorMap& tmQ,
+                             const CUtensorMap& tmK, const CUtensorMap& tmV, dim3 grid,
+                             cudaStream_t stream);
+cudaError_t launch_umma_e4m3(int d_qk, int d_v, const FwdParams& p, const CUtensorMap& tmQ,
+                             const CUtensorMap& tmK, const CUtensorMap& tmV, dim3 grid,
+                             cudaStream_t stream);
+
 // Launch the split combine (one warp per output row).
 cudaError_t launch_combine(const FwdParams& p, cudaStream_t stream);
 

@@ -1,0 +1,448 @@
+// Tensor-core split-KV partial kernel (tcgen05 + TMEM + TMA) for tiles with
+// many query rows per KV head: short cached-prefix queries, GQA groups of
+// eight or more, varlen prefill.
+//
+// flash-attention PR "[Cute,Fwd,Sm100] Support q_stage=1 for inference":
+// the Blackwell MMA has M = 128 and a CTA holding one 128-row query tile
+// (q_stage = 1) is what short-query split-KV needs; the GQA query rows of a
+// KV head are packed into that tile (row r = query r / group, head r % group)
+// so few queries still fill it.
+//
+// One CTA = one (128-row tile, sequence * KV head, split); 6 warps:
+//   warp 0      TMA producer: Q tile once, then K and V tiles of 128 keys
+//               through a STAGES-deep ring (separate K/V full barriers, one
+//               empty barrier per stage released by an MMA commit);
+//   warp 1      allocates 512 TMEM columns; lane 0 issues the MMAs:
+//               S_j = Q K_j^T into one of two TMEM S buffers (ping-pong, so
+//               S_{j+1} overlaps the softmax of S_j), then O += P_j V_j into
+//               the TMEM O accumulator;
+//   warps 2-5   one thread per query row (TMEM lane): load the S row, apply
+//               the residual / bottom-right causal / window mask, online
+//               softmax in the exp2 domain, rescale the O row in TMEM when
+//               the running max moves, write P (bf16 / fp16 / e4m3, 128B
+//               swizzled K-major) to shared memory, and finally normalise O
+//               and store it (or the fp32 split partial) with row-predicated
+//               vector stores (cutlass "Adds variable sequence lengths to the
+//               Hopper CuTe DSL FMHA example", "Implementation": rows past a
+//               sequence are computed but never stored).
+//
+// Operand layouts (all 128B-swizzled, 1024-byte aligned, 128-byte rows):
+//   Q  [128 rows][d_qk]  K-major A of S      K [128 keys][d_qk]  K-major B of S
+//   P  [128 rows][128 keys] K-major A of PV  V [128 keys][d_v]   MN-major B of PV
+// each split into 128-byte-wide panels of 128 rows (16 KB).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp8.h>
+#include <math_constants.h>
+
+#include "fa_common.cuh"
+#include "fa_convert.cuh"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+template <int DT, int DQK, int DV, int STAGES>
+struct UmmaCfg {
+  static constexpr int ES = Elem<DT>::size;
+  static constexpr int PANEL_ELEMS = 128 / ES;
+  static constexpr int PANEL = 128 * 128;                  // 128 rows x 128 bytes
+  static constexpr int NPQ = (DQK * ES + 127) / 128;       // panels of Q / K
+  static constexpr int NPV = (DV * ES + 127) / 128;        // panels of V
+  static constexpr int NPP = ES;                           // panels of P (128 keys)
+  static constexpr int UMMA_K = 32 / ES;                   // K elements per MMA
+  static constexpr int KSTEPS_PER_PANEL = PANEL_ELEMS / UMMA_K;
+  static constexpr int S_KSTEPS = (DQK + UMMA_K - 1) / UMMA_K;
+  static constexpr int PV_KSTEPS = 128 / UMMA_K;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int TM_S0 = 0, TM_S1 = 128, TM_O = 256;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = OFF_Q + NPQ * PANEL;
+  static constexpr int KV_STAGE = (NPQ + NPV) * PANEL;
+  static constexpr int OFF_P = OFF_KV + STAGES * KV_STAGE;
+  static constexpr int OFF_BAR = OFF_P + NPP * PANEL;
+  // barriers: q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_ready, o_ready, drain
+  static constexpr int NBAR = 1 + 3 * STAGES + 2 + 3;
+  static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_FLAG = OFF_TMEM_SLOT + 16;
+  static constexpr int SMEM = OFF_FLAG + 16 + 1024;
+  static constexpr int NTHREADS = 192;
+  static constexpr uint32_t IDESC_S =
+      mma_idesc(DT == kBF16 ? 1u : 0u, 128, 128, 0, 0);    // Q K^T: both K-major
+  static constexpr uint32_t IDESC_PV =
+      mma_idesc(DT == kBF16 ? 1u : 0u, 128, DV, 0, 1);     // P V: V is MN-major
+  static_assert(DV <= 256 && DV % 16 == 0, "d_v");
+  static_assert(TM_O + DV <= TMEM_COLS, "TMEM columns");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+template <int DT>
+__device__ __forceinline__ void mma_issue(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t acc) {
+  if constexpr (DT == kE4M3)
+    tc_mma_f8(d, a, b, idesc, acc);
+  else
+    tc_mma_f16(d, a, b, idesc, acc);
+}
+
+// Packs 8 probabilities into 16 bytes of P (16-bit types) or 16 into 16
+// bytes (e4m3, pre-scaled by 256 so small values stay representable).
+template <int DT>
+__device__ __forceinline__ uint4 pack_p16(const float* p);
+
+template <>
+__device__ __forceinline__ uint4 pack_p16<kBF16>(const float* p) {
+  return make_uint4(pack2(p[0], p[1], kBF16), pack2(p[2], p[3], kBF16), pack2(p[4], p[5], kBF16),
+                    pack2(p[6], p[7], kBF16));
+}
+template <>
+__device__ __forceinline__ uint4 pack_p16<kFP16>(const float* p) {
+  return make_uint4(pack2(p[0], p[1], kFP16), pack2(p[2], p[3], kFP16), pack2(p[4], p[5], kFP16),
+                    pack2(p[6], p[7], kFP16));
+}
+template <>
+__device__ __forceinline__ uint4 pack_p16<kE4M3>(const float* p) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_fp8x2_storage_t lo =
+        __nv_cvt_float2_to_fp8x2(make_float2(p[4 * i] * 256.f, p[4 * i + 1] * 256.f), __NV_SATFINITE,
+                                 __NV_E4M3);
+    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+        make_float2(p[4 * i + 2] * 256.f, p[4 * i + 3] * 256.f), __NV_SATFINITE, __NV_E4M3);
+    w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <int DT, int DQK, int DV, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    umma_splitkv_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV) {
+  using C = UmmaCfg<DT, DQK, DV, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t pad = ((raw_u32 + 1023u) & ~1023u) - raw_u32;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw_u32 + pad;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // Heaviest tiles first: with causal masks later query tiles see more keys.
+  const int m_blk = gridDim.x - 1 - blockIdx.x;
+  const int b = blockIdx.y / p.h_kv;
+  const int kh = blockIdx.y - b * p.h_kv;
+  const int split = blockIdx.z;
+  const int group = p.group;
+  const int qpt = 128 / group;  // queries per tile
+
+  if (timed_out_before(p.err)) return;
+  SeqInfo sq;
+  if (!load_seq(p, b, sq)) {
+    if (threadIdx.x == 0) record_error(p.err, kErrDeviceArg);
+    return;
+  }
+  const int q_start = m_blk * qpt;
+  if (q_start >= sq.lq) return;  // tile past this sequence's queries
+  const int nq = min(qpt, sq.lq - q_start);
+  const int nrows = nq * group;
+  int k0, k1;
+  tile_split_range(q_start, q_start + nq - 1, sq.lq, sq.lk, p.causal, p.window_left, p.num_splits,
+                   split, k0, k1);
+  const int nblk = k1 > k0 ? (k1 - k0 + kBlockN - 1) / kBlockN : 0;
+
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  const uint32_t q_full = bar0;
+  const uint32_t k_full = bar0 + 8;                  // [STAGES]
+  const uint32_t v_full = k_full + 8 * STAGES;       // [STAGES]
+  const uint32_t kv_empty = v_full + 8 * STAGES;     // [STAGES]
+  const uint32_t s_full = kv_empty + 8 * STAGES;     // [2]
+  const uint32_t p_ready = s_full + 16;
+  const uint32_t o_ready = p_ready + 8;
+  const uint32_t drain = o_ready + 8;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(k_full + 8 * s, 1);
+      mbar_init(v_full + 8 * s, 1);
+      mbar_init(kv_empty + 8 * s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_full + 8, 1);
+    mbar_init(p_ready, 128);
+    mbar_init(o_ready, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + C::OFF_TMEM_SLOT, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  int issued_kv = 0;  // producer: K/V stages issued
+
+  if (warp == 0) {
+    // -------------------------------------------------------------- producer
+    if (lane == 0 && nblk > 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const uint64_t pol_q = l2_policy_evict_first();
+      const uint64_t pol_kv = gridDim.x == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
+      mbar_arrive_expect_tx(q_full, C::NPQ * qpt * group * 128);
+#pragma unroll
+      for (int pq = 0; pq < C::NPQ; ++pq)
+        tma_load_3d(sbase + C::OFF_Q + pq * C::PANEL, &tmQ, q_full, pq * C::PANEL_ELEMS,
+                    kh * group, sq.q0 + q_start, pol_q);
+      for (int j = 0; j < nblk; ++j) {
+        const int st = j % STAGES;
+        if (j >= STAGES && !mbar_wait(kv_empty + 8 * st, ((j / STAGES) - 1) & 1, p.err, abort_flag))
+          break;
+        const uint32_t kdst = sbase + C::OFF_KV + st * C::KV_STAGE;
+        const uint32_t vdst = kdst + C::NPQ * C::PANEL;
+        const int row = sq.k0 + k0 + j * kBlockN;
+        mbar_arrive_expect_tx(k_full + 8 * st, C::NPQ * C::PANEL);
+#pragma unroll
+        for (int pk = 0; pk < C::NPQ; ++pk)
+          tma_load_3d(kdst + pk * C::PANEL, &tmK, k_full + 8 * st, pk * C::PANEL_ELEMS, kh, row,
+                      pol_kv);
+        mbar_arrive_expect_tx(v_full + 8 * st, C::NPV * C::PANEL);
+#pragma unroll
+        for (int pv = 0; pv < C::NPV; ++pv)
+          tma_load_3d(vdst + pv * C::PANEL, &tmV, v_full + 8 * st, pv * C::PANEL_ELEMS, kh, row,
+                      pol_kv);
+        issued_kv = j + 1;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0 && nblk > 0) {
+      bool ok = mbar_wait(q_full, 0, p.err, abort_flag);
+      const uint32_t q_addr = sbase + C::OFF_Q;
+      const uint32_t p_addr = sbase + C::OFF_P;
+      auto issue_s = [&](int j) {
+        const int st = j % STAGES;
+        const uint32_t k_addr = sbase + C::OFF_KV + st * C::KV_STAGE;
+        const uint32_t d = tmem + ((j & 1) ? C::TM_S1 : C::TM_S0);
+#pragma unroll
+        for (int ks = 0; ks < C::S_KSTEPS; ++ks) {
+          const uint32_t off = (ks / C::KSTEPS_PER_PANEL) * C::PANEL + (ks % C::KSTEPS_PER_PANEL) * 32;
+          mma_issue<DT>(d, smem_desc_sw128(q_addr + off, 16, 1024),
+                        smem_desc_sw128(k_addr + off, 16, 1024), C::IDESC_S, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(s_full + 8 * (j & 1));
+      };
+      if (ok) ok = mbar_wait(k_full, 0, p.err, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      for (int j = 0; ok && j < nblk; ++j) {
+        const int st = j % STAGES;
+        if (j + 1 < nblk) {
+          const int st1 = (j + 1) % STAGES;
+          ok = mbar_wait(k_full + 8 * st1, ((j + 1) / STAGES) & 1, p.err, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(j + 1);
+        }
+        ok = mbar_wait(p_ready, j & 1, p.err, abort_flag) &&
+             mbar_wait(v_full + 8 * st, (j / STAGES) & 1, p.err, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t v_addr = sbase + C::OFF_KV + st * C::KV_STAGE + C::NPQ * C::PANEL;
+#pragma unroll
+        for (int ks = 0; ks < C::PV_KSTEPS; ++ks) {
+          const uint32_t a_off =
+              (ks / C::KSTEPS_PER_PANEL) * C::PANEL + (ks % C::KSTEPS_PER_PANEL) * 32;
+          const uint32_t b_off = ks * C::UMMA_K * 128;
+          mma_issue<DT>(tmem + C::TM_O, smem_desc_sw128(p_addr + a_off, 16, 1024),
+                        smem_desc_sw128(v_addr + b_off, C::PANEL, 1024), C::IDESC_PV,
+                        (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc_commit(o_ready);
+        tc_commit(kv_empty + 8 * st);
+      }
+      // Let every issued MMA finish before TMEM can be released.
+      tc_commit(drain);
+      mbar_wait(drain, 0, nullptr, nullptr);
+    }
+  } else {
+    // ----------------------------------------------------- softmax warps
+    const int quarter = warp & 3;          // TMEM lane quarter of this warp
+    const int r = quarter * 32 + lane;     // tile row = TMEM lane
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const bool row_ok = r < nrows;
+    const bool warp_active = quarter * 32 < nrows;
+    const int i = q_start + r / group;
+    const int h = kh * group + (r - (r / group) * group);
+    int lo = 0, hi = 0;
+    if (row_ok) {
+      row_key_range(i, sq.lq, sq.lk, p.causal, p.window_left, lo, hi);
+      lo = max(lo, k0);
+      hi = min(hi, k1);
+    }
+    float sl2 = p.scale * 1.4426950408889634f;
+    if (DT == kE4M3) sl2 *= __ldg(p.descale_q) * __ldg(p.descale_k);
+    float m_run = -CUDART_INF_F, l_run = 0.f;
+    uint8_t* p_row = smem + C::OFF_P + r * 128;
+    bool ok = true;
+
+    for (int j = 0; j < nblk; ++j) {
+      float s[128];
+      float m_new = m_run;
+      if (warp_active) {
+        ok = mbar_wait(s_full + 8 * (j & 1), (j >> 1) & 1, p.err, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+        const uint32_t s_addr = tmem + lane_base + ((j & 1) ? C::TM_S1 : C::TM_S0);
+        const int kb = k0 + j * kBlockN;
+        float bmax = -CUDART_INF_F;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t raw[32];
+          tmem_ld32(s_addr + 32 * c4, raw);
+#pragma unroll
+          for (int t = 0; t < 32; ++t) {
+            const int key = kb + 32 * c4 + t;
+            const float x =
+                (key >= lo && key < hi) ? __uint_as_float(raw[t]) * sl2 : -CUDART_INF_F;
+            s[32 * c4 + t] = x;
+            bmax = fmaxf(bmax, x);
+          }
+        }
+        m_new = fmaxf(m_run, bmax);
+      }
+      // PV of the previous block must be done before O is rescaled and the
+      // P buffer is overwritten.
+      if (j > 0) {
+        ok = mbar_wait(o_ready, (j - 1) & 1, p.err, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+      }
+      if (warp_active) {
+        const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
+        // alpha rescales what was accumulated so far; a row that has seen no
+        // key yet holds O = 0 and l = 0, so it needs no rescale.
+        const float alpha = m_run == m_new ? 1.f : fast_exp2(m_run - m_use);
+        float rsum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const float e = fast_exp2(s[c] - m_use);  // masked: exp2(-inf) = 0
+          s[c] = e;
+          rsum += e;
+        }
+        const bool rescale = j > 0 && m_run != -CUDART_INF_F && alpha != 1.f;
+        if (__any_sync(0xffffffffu, rescale)) {
+          const uint32_t o_addr = tmem + lane_base + C::TM_O;
+#pragma unroll
+          for (int c = 0; c < DV / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(o_addr + 32 * c, o);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+            tmem_st32(o_addr + 32 * c, o);
+          }
+          tmem_st_wait();
+        }
+        l_run = l_run * alpha + rsum;
+        m_run = m_new;
+        // P row, 128B-swizzled K-major: 16-byte chunk c of panel pp at
+        // position c ^ (r % 8).
+        constexpr int EPC = 16 / C::ES;  // P elements per 16-byte chunk
+#pragma unroll
+        for (int c = 0; c < 128 / EPC; ++c) {
+          const int pp = c / 8, cc = c % 8;
+          const uint4 w = pack_p16<DT>(s + c * EPC);
+          *reinterpret_cast<uint4*>(p_row + pp * C::PANEL + ((cc ^ (r & 7)) << 4)) = w;
+        }
+        fence_proxy_async_smem();
+      }
+      tc_fence_before();
+      mbar_arrive(p_ready);
+    }
+
+    // ------------------------------------------------------------ epilogue
+    if (ok && nblk > 0) {
+      ok = mbar_wait(o_ready, (nblk - 1) & 1, p.err, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+    }
+    if (warp_active && ok) {
+      float inv = 0.f, lse_v = -CUDART_INF_F;
+      if (row_ok && l_run > 0.f && m_run != -CUDART_INF_F) {
+        inv = 1.f / l_run;
+        if (DT == kE4M3) inv *= __ldg(p.descale_v) * (1.f / 256.f);
+        lse_v = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+      }
+      const int t = sq.q0 + i;
+      const uint32_t o_addr = tmem + lane_base + C::TM_O;
+#pragma unroll
+      for (int c = 0; c < DV / 32; ++c) {
+        uint32_t o[32];
+        if (nblk > 0) {
+          tmem_ld32(o_addr + 32 * c, o);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+        if (!row_ok) continue;
+        float f[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(o[e]) * inv;
+        if (p.num_splits == 1) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) +
+                                                ((size_t)t * p.h_q + h) * (size_t)DV * 2 + c * 64);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(pack2(f[8 * e], f[8 * e + 1], p.out_dtype),
+                                pack2(f[8 * e + 2], f[8 * e + 3], p.out_dtype),
+                                pack2(f[8 * e + 4], f[8 * e + 5], p.out_dtype),
+                                pack2(f[8 * e + 6], f[8 * e + 7], p.out_dtype));
+        } else {
+          const size_t slot = (size_t)b * p.max_seqlen_q + i;
+          float4* dst = reinterpret_cast<float4*>(
+              p.ws_o + (((size_t)split * p.slots + slot) * p.h_q + h) * DV + c * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) dst[e] = make_float4(f[4 * e], f[4 * e + 1], f[4 * e + 2], f[4 * e + 3]);
+        }
+      }
+      if (row_ok) {
+        if (p.num_splits == 1) {
+          if (p.lse != nullptr) p.lse[(size_t)h * p.total_q + t] = lse_v;
+        } else {
+          const size_t slot = (size_t)b * p.max_seqlen_q + i;
+          p.ws_l[((size_t)split * p.slots + slot) * p.h_q + h] = lse_v;
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------- teardown
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    // let issued loads land before the CTA's shared memory is released
+    for (int st = 0; st < STAGES && st < issued_kv; ++st) {
+      const int j_last = st + ((issued_kv - 1 - st) / STAGES) * STAGES;
+      mbar_wait(k_full + 8 * st, (j_last / STAGES) & 1, nullptr, nullptr);
+      mbar_wait(v_full + 8 * st, (j_last / STAGES) & 1, nullptr, nullptr);
+    }
+    if (nblk > 0) mbar_wait(q_full, 0, nullptr, nullptr);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace fa

@@ -14,7 +14,7 @@ from workloads import cu_seqlens, gqa_decode_lengths, make_inputs, workload
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = [fa.FA_KERNEL_SIMT]
+KERNELS = [fa.FA_KERNEL_SIMT, fa.FA_KERNEL_UMMA]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -255,4 +255,26 @@ def test_full_fp8_cached_prefix(kv):
     inp = workload("fp8_prefix", kv=kv, device="cuda")
     out, lse = run_gpu(inp)
     o_ref, l_ref = reference(inp)
+    assert_close(inp, out, lse, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("h_kv,causal", [(16, False), (16, True), (4, False), (4, True)])
+def test_full_varlen_prefill_sampled_heads(dtype, h_kv, causal):
+    """16384 packed tokens (4096, 512, 3072, 1024, 2560, 1536, 2048, 1536),
+    H_q=16, D=128, automatic kernel and splits; 2 query heads checked."""
+    inp = workload("prefill", dtype=dtype, h_kv=h_kv, device="cuda")
+    out, lse = run_gpu(inp, causal=causal)
+    heads = [0, 13]
+    o_ref, l_ref = reference(inp, 0.0, causal, heads=heads)
+    assert_close(inp, out, lse, o_ref, l_ref, heads=heads)
+    assert np.isfinite(out).all()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_gqa_group_16_prefix(kernel):
+    """Group 16: eight queries per 128-row tile share one KV head."""
+    inp = make_inputs([20, 9], [700, 260], 32, 2, 128, 128, "bf16", seed=9)
+    out, lse = run_gpu(inp, num_splits=0, flags=kernel, causal=True)
+    o_ref, l_ref = reference(inp, 0.0, True)
     assert_close(inp, out, lse, o_ref, l_ref)

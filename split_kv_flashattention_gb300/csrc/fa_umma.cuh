@@ -86,7 +86,18 @@ __device__ __forceinline__ void mma_issue(uint32_t d, uint64_t a, uint64_t b, ui
 }
 
 // Packs 8 probabilities into 16 bytes of P (16-bit types) or 16 into 16
-// bytes (e4m3, pre-scaled by 256 so small values stay representable).
+// bytes (e4m3).  With the lazy rescale below a probability is at most
+// 2^kLazy[DT]; e4m3 P is scaled by kP8Scale = 2^(8 - 4) so it stays within
+// e4m3's range (448) while small values keep their leading bits.
+// Lazy rescale threshold (log2 units): the running max used for the
+// exponentials is only raised when a row's true max exceeds it by more
+// than this, so O in TMEM is rarely rescaled.
+template <int DT>
+struct Lazy {
+  static constexpr float kThreshold = DT == kE4M3 ? 4.f : 8.f;
+};
+constexpr float kP8Scale = 16.f;
+
 template <int DT>
 __device__ __forceinline__ uint4 pack_p16(const float* p);
 
@@ -106,10 +117,10 @@ __device__ __forceinline__ uint4 pack_p16<kE4M3>(const float* p) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const __nv_fp8x2_storage_t lo =
-        __nv_cvt_float2_to_fp8x2(make_float2(p[4 * i] * 256.f, p[4 * i + 1] * 256.f), __NV_SATFINITE,
-                                 __NV_E4M3);
+        __nv_cvt_float2_to_fp8x2(make_float2(p[4 * i] * kP8Scale, p[4 * i + 1] * kP8Scale),
+                                 __NV_SATFINITE, __NV_E4M3);
     const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-        make_float2(p[4 * i + 2] * 256.f, p[4 * i + 3] * 256.f), __NV_SATFINITE, __NV_E4M3);
+        make_float2(p[4 * i + 2] * kP8Scale, p[4 * i + 3] * kP8Scale), __NV_SATFINITE, __NV_E4M3);
     w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
@@ -300,47 +311,59 @@ __global__ void __launch_bounds__(192, 1)
     for (int j = 0; j < nblk; ++j) {
       float s[128];
       float m_new = m_run;
+      float alpha = 1.f, rsum = 0.f;
       if (warp_active) {
         ok = mbar_wait(s_full + 8 * (j & 1), (j >> 1) & 1, p.err, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
         const uint32_t s_addr = tmem + lane_base + ((j & 1) ? C::TM_S1 : C::TM_S0);
         const int kb = k0 + j * kBlockN;
-        float bmax = -CUDART_INF_F;
+        tmem_ld64(s_addr, reinterpret_cast<uint32_t*>(s));
+        tmem_ld64(s_addr + 64, reinterpret_cast<uint32_t*>(s) + 64);
+        // Max of the raw scores (the scale is positive): eight independent
+        // chains; keys outside [lo, hi) only exist in boundary blocks.
+        float mx[8];
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t raw[32];
-          tmem_ld32(s_addr + 32 * c4, raw);
+        for (int t = 0; t < 8; ++t) mx[t] = -CUDART_INF_F;
+        if (kb >= lo && kb + kBlockN <= hi) {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) {
-            const int key = kb + 32 * c4 + t;
-            const float x =
-                (key >= lo && key < hi) ? __uint_as_float(raw[t]) * sl2 : -CUDART_INF_F;
-            s[32 * c4 + t] = x;
-            bmax = fmaxf(bmax, x);
+          for (int c = 0; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const int key = kb + c;
+            s[c] = (key >= lo && key < hi) ? s[c] : -CUDART_INF_F;
+            mx[c & 7] = fmaxf(mx[c & 7], s[c]);
           }
         }
-        m_new = fmaxf(m_run, bmax);
+        const float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+        // Lazy rescale: keep the max in use unless the block's max exceeds
+        // it by more than the threshold (probabilities then stay <= 2^thr).
+        m_new = (bmax > m_run + Lazy<DT>::kThreshold) ? bmax : m_run;
+        const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
+        // alpha rescales what was accumulated so far; a row that has seen no
+        // key yet holds O = 0 and l = 0, so it needs no rescale.
+        alpha = m_run == m_new ? 1.f : fast_exp2(m_run - m_use);
+        float sm[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) sm[t] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const float e = fast_exp2(fmaf(s[c], sl2, -m_use));  // masked: exp2(-inf) = 0
+          s[c] = e;
+          sm[c & 7] += e;
+        }
+        rsum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
       }
       // PV of the previous block must be done before O is rescaled and the
-      // P buffer is overwritten.
+      // P buffer is overwritten (the exponentials above overlap it).
       if (j > 0) {
         ok = mbar_wait(o_ready, (j - 1) & 1, p.err, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
       }
       if (warp_active) {
-        const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
-        // alpha rescales what was accumulated so far; a row that has seen no
-        // key yet holds O = 0 and l = 0, so it needs no rescale.
-        const float alpha = m_run == m_new ? 1.f : fast_exp2(m_run - m_use);
-        float rsum = 0.f;
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const float e = fast_exp2(s[c] - m_use);  // masked: exp2(-inf) = 0
-          s[c] = e;
-          rsum += e;
-        }
         const bool rescale = j > 0 && m_run != -CUDART_INF_F && alpha != 1.f;
         if (__any_sync(0xffffffffu, rescale)) {
           const uint32_t o_addr = tmem + lane_base + C::TM_O;
@@ -381,7 +404,7 @@ __global__ void __launch_bounds__(192, 1)
       float inv = 0.f, lse_v = -CUDART_INF_F;
       if (row_ok && l_run > 0.f && m_run != -CUDART_INF_F) {
         inv = 1.f / l_run;
-        if (DT == kE4M3) inv *= __ldg(p.descale_v) * (1.f / 256.f);
+        if (DT == kE4M3) inv *= __ldg(p.descale_v) * (1.f / kP8Scale);
         lse_v = (m_run + __log2f(l_run)) * 0.69314718055994531f;
       }
       const int t = sq.q0 + i;

@@ -137,7 +137,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="long_decode", choices=sorted(WORKLOADS))
     ap.add_argument("--num-splits", type=int, default=0)
-    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "umma"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "umma", "umma2"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the varlen prefill TFLOPS measurement of the default line")
@@ -177,6 +177,8 @@ KERNEL_SOURCES = {
                      "fa_ptx.cuh", "fa_convert.cuh"),
     "umma_splitkv": ("fa_umma.cuh", "fa_umma_launch.cuh", "fa_umma_bf16.cu", "fa_umma_e4m3.cu",
                      "fa_common.cuh", "fa_ptx.cuh", "fa_convert.cuh"),
+    "umma2_splitkv": ("fa_umma2.cuh", "fa_umma2_launch.cuh", "fa_umma2_bf16.cu", "fa_common.cuh",
+                      "fa_ptx.cuh", "fa_convert.cuh"),
 }
 
 
@@ -357,7 +359,7 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
 
     kernel_flag = {"auto": fa.FA_KERNEL_AUTO, "simt": fa.FA_KERNEL_SIMT,
-                   "umma": fa.FA_KERNEL_UMMA}[args.kernel]
+                   "umma": fa.FA_KERNEL_UMMA, "umma2": fa.FA_KERNEL_UMMA2}[args.kernel]
     kw = dict(spec["kw"])
     if args.kv:
         kw["kv"] = args.kv
@@ -378,9 +380,14 @@ def main():
         dv = torch.tensor([inp.descale_v], dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     rows = inp.max_seqlen_q * (inp.h_q // inp.h_kv)
-    uses_umma = args.kernel == "umma" or (args.kernel == "auto" and rows > (2 if (
-        inp.dtype == "e4m3" and inp.d_qk == 192) else 4))
-    kern_tag = "umma_splitkv" if uses_umma else "simt_splitkv"
+    simt_rows = 2 if (inp.dtype == "e4m3" and inp.d_qk == 192) else 4
+    if args.kernel == "auto":
+        if rows <= simt_rows:
+            kern_tag = "simt_splitkv"
+        else:
+            kern_tag = "umma_splitkv"
+    else:
+        kern_tag = {"simt": "simt_splitkv", "umma": "umma_splitkv", "umma2": "umma2_splitkv"}[args.kernel]
 
     def call(flags):
         fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, inp.max_seqlen_q, out, lse, ws, 0.0, causal, -1,

@@ -76,9 +76,10 @@ typedef enum {
 } fa_status;
 
 /* Kernel selection (flags argument of fa_fwd_splitkv_ex). */
-#define FA_KERNEL_AUTO 0 /* by rows per KV head: CUDA-core for few, tcgen05 else */
-#define FA_KERNEL_SIMT 1 /* CUDA-core streaming kernel                          */
-#define FA_KERNEL_UMMA 2 /* tcgen05 tensor-core kernel                          */
+#define FA_KERNEL_AUTO 0  /* by rows per KV head (see fa_fwd_splitkv_ex)            */
+#define FA_KERNEL_SIMT 1  /* CUDA-core streaming kernel                            */
+#define FA_KERNEL_UMMA 2  /* tcgen05 kernel, one 128-row query tile per CTA        */
+#define FA_KERNEL_UMMA2 3 /* tcgen05 kernel, two 128-row tiles per CTA (16-bit)    */
 #define FA_KERNEL_MASK 3
 /* Stage selection (flags, OR-ed with the kernel choice).  By default a call
  * launches the partial kernel and, when the split count is > 1, the combine.
@@ -117,7 +118,11 @@ typedef enum {
  *                 fp16 (equal to in_dtype for 16-bit inputs).
  *  descale_q/k/v  device float32 scalars, required for FA_E4M3 inputs
  *                 (per-tensor dequantisation factors), ignored otherwise.
- *  flags          FA_KERNEL_* selection, optionally OR FA_RUN_*_ONLY.
+ *  flags          FA_KERNEL_* selection, optionally OR FA_RUN_*_ONLY.  AUTO
+ *                 picks the CUDA-core kernel for up to 4 rows (queries x
+ *                 group) per KV head (2 for e4m3 with d_qk=192) and the
+ *                 one-tile tcgen05 kernel beyond; the two-tile kernel is
+ *                 only used when requested.
  *  stream         cudaStream_t.
  * Returns FA_OK or a negative fa_status.
  */

@@ -21,13 +21,13 @@ __all__ = [
     "FaError", "FaLibraryMissing", "library", "fa_fwd_splitkv_ex", "fa_fwd_splitkv",
     "fa_fwd_splitkv_workspace_size", "fa_plan", "fa_debug_split_ranges",
     "fa_get_device_error", "fa_status_string", "fa_version", "forward",
-    "FA_KERNEL_AUTO", "FA_KERNEL_SIMT", "FA_KERNEL_UMMA", "FA_RUN_PARTIAL_ONLY",
+    "FA_KERNEL_AUTO", "FA_KERNEL_SIMT", "FA_KERNEL_UMMA", "FA_KERNEL_UMMA2", "FA_RUN_PARTIAL_ONLY",
     "FA_RUN_COMBINE_ONLY", "DTYPE_CODES", "fa_fwd_splitkv_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libfa_splitkv.so")
 
-FA_KERNEL_AUTO, FA_KERNEL_SIMT, FA_KERNEL_UMMA = 0, 1, 2
+FA_KERNEL_AUTO, FA_KERNEL_SIMT, FA_KERNEL_UMMA, FA_KERNEL_UMMA2 = 0, 1, 2, 3
 FA_RUN_PARTIAL_ONLY, FA_RUN_COMBINE_ONLY = 4, 8
 DTYPE_CODES = {torch.bfloat16: 0, torch.float16: 1, torch.float8_e4m3fn: 2}
 EXPORTED = (

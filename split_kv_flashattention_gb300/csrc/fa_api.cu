@@ -297,7 +297,7 @@ int fa_fwd_splitkv_ex(const void* q, const void* k, const void* v, const int* cu
   if (!dims_supported(in_dtype, d_qk, d_v)) return FA_ERR_UNSUPPORTED;
   if (isnan(scale) || isinf(scale)) return FA_ERR_INVALID_ARG;
   const int kernel_sel = flags & FA_KERNEL_MASK;
-  if (kernel_sel == FA_KERNEL_MASK) return FA_ERR_INVALID_ARG;
+  if (kernel_sel == FA_KERNEL_UMMA2 && in_dtype == kE4M3) return FA_ERR_UNSUPPORTED;
   if (flags & ~(FA_KERNEL_MASK | FA_RUN_PARTIAL_ONLY | FA_RUN_COMBINE_ONLY)) return FA_ERR_INVALID_ARG;
   const bool run_partial = !(flags & FA_RUN_COMBINE_ONLY);
   const bool run_combine = !(flags & FA_RUN_PARTIAL_ONLY);
@@ -369,18 +369,31 @@ int fa_fwd_splitkv_ex(const void* q, const void* k, const void* v, const int* cu
   // cores; more rows form a dense contraction for the tensor cores.
   const int rows = max_seqlen_q * p.group;
   const int rt_max = simt_max_rows(in_dtype, d_qk, d_v);
-  const bool use_umma =
-      kernel_sel == FA_KERNEL_UMMA || (kernel_sel == FA_KERNEL_AUTO && rows > rt_max);
+  const bool auto_tc = kernel_sel == FA_KERNEL_AUTO && rows > rt_max;
+  // The one-tile kernel is the faster tensor-core path on GB300 for every
+  // measured shape, so AUTO uses it; the two-tile kernel is selected
+  // explicitly.
+  const bool use_umma2 = kernel_sel == FA_KERNEL_UMMA2;
+  const bool use_umma = !use_umma2 && (kernel_sel == FA_KERNEL_UMMA || auto_tc);
   if ((unsigned)(batch * h_kv) > 65535u) return FA_ERR_UNSUPPORTED;
   if (run_partial) {
     CUtensorMap tmK, tmV;
-    const int box_keys = use_umma ? kBlockN : 32;
+    const int box_keys = (use_umma || use_umma2) ? kBlockN : 32;
     st = make_tmap_3d(&tmK, k, in_dtype, d_qk, h_kv, total_k, box_keys);
     if (st != FA_OK) return st;
     st = make_tmap_3d(&tmV, v, in_dtype, d_v, h_kv, total_k, box_keys);
     if (st != FA_OK) return st;
     cudaError_t e;
-    if (use_umma) {
+    if (use_umma2) {
+      const int qpt = 128 / p.group;
+      p.tile_rows = 2 * qpt * p.group;
+      CUtensorMap tmQ;
+      st = make_tmap_3d(&tmQ, q, in_dtype, d_qk, h_q, total_q, qpt, p.group);
+      if (st != FA_OK) return st;
+      dim3 grid((unsigned)ceil_div(max_seqlen_q, 2 * qpt), (unsigned)(batch * h_kv), (unsigned)ns);
+      e = in_dtype == kFP16 ? launch_umma2_fp16(d_qk, d_v, p, tmQ, tmK, tmV, grid, s)
+                            : launch_umma2_bf16(d_qk, d_v, p, tmQ, tmK, tmV, grid, s);
+    } else if (use_umma) {
       const int qpt = 128 / p.group;
       p.tile_rows = qpt * p.group;
       CUtensorMap tmQ;

@@ -38,6 +38,15 @@ cudaError_t launch_umma_e4m3(int d_qk, int d_v, const FwdParams& p, const CUtens
                              const CUtensorMap& tmK, const CUtensorMap& tmV, dim3 grid,
                              cudaStream_t stream);
 
+// Launch the two-tile (256-row) tcgen05 split kernel (16-bit inputs).
+// grid = (query tile pairs, batch*h_kv, ns).
+cudaError_t launch_umma2_bf16(int d_qk, int d_v, const FwdParams& p, const CUtensorMap& tmQ,
+                              const CUtensorMap& tmK, const CUtensorMap& tmV, dim3 grid,
+                              cudaStream_t stream);
+cudaError_t launch_umma2_fp16(int d_qk, int d_v, const FwdParams& p, const CUtensorMap& tmQ,
+                              const CUtensorMap& tmK, const CUtensorMap& tmV, dim3 grid,
+                              cudaStream_t stream);
+
 // Launch the split combine (one warp per output row).
 cudaError_t launch_combine(const FwdParams& p, cudaStream_t stream);
 

@@ -10,8 +10,10 @@
 //
 // One CTA = one (128-row tile, sequence * KV head, split); 6 warps:
 //   warp 0      TMA producer: Q tile once, then K and V tiles of 128 keys
-//               through a STAGES-deep ring (separate K/V full barriers, one
-//               empty barrier per stage released by an MMA commit);
+//               through separate rings (KS deep for K, VS for V).  A K stage
+//               is released as soon as its S MMA completes, so K runs ahead
+//               of V: loads for block j+2 are in flight while block j's
+//               softmax and PV run, which hides the L2/HBM latency;
 //   warp 1      allocates 512 TMEM columns; lane 0 issues the MMAs:
 //               S_j = Q K_j^T into one of two TMEM S buffers (ping-pong, so
 //               S_{j+1} overlaps the softmax of S_j), then O += P_j V_j into
@@ -42,7 +44,7 @@
 
 namespace fa {
 
-template <int DT, int DQK, int DV, int STAGES>
+template <int DT, int DQK, int DV, int KS, int VS>
 struct UmmaCfg {
   static constexpr int ES = Elem<DT>::size;
   static constexpr int PANEL_ELEMS = 128 / ES;
@@ -57,12 +59,15 @@ struct UmmaCfg {
   static constexpr int TMEM_COLS = 512;
   static constexpr int TM_S0 = 0, TM_S1 = 128, TM_O = 256;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = OFF_Q + NPQ * PANEL;
-  static constexpr int KV_STAGE = (NPQ + NPV) * PANEL;
-  static constexpr int OFF_P = OFF_KV + STAGES * KV_STAGE;
+  static constexpr int K_STAGE = NPQ * PANEL;
+  static constexpr int V_STAGE = NPV * PANEL;
+  static constexpr int OFF_K = OFF_Q + NPQ * PANEL;
+  static constexpr int OFF_V = OFF_K + KS * K_STAGE;
+  static constexpr int OFF_P = OFF_V + VS * V_STAGE;
   static constexpr int OFF_BAR = OFF_P + NPP * PANEL;
-  // barriers: q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_ready, o_ready, drain
-  static constexpr int NBAR = 1 + 3 * STAGES + 2 + 3;
+  // barriers: q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2],
+  // p_ready, o_ready, drain
+  static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 2 + 3;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_FLAG = OFF_TMEM_SLOT + 16;
   static constexpr int SMEM = OFF_FLAG + 16 + 1024;
@@ -126,12 +131,12 @@ __device__ __forceinline__ uint4 pack_p16<kE4M3>(const float* p) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-template <int DT, int DQK, int DV, int STAGES>
+template <int DT, int DQK, int DV, int KS, int VS>
 __global__ void __launch_bounds__(192, 1)
     umma_splitkv_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV) {
-  using C = UmmaCfg<DT, DQK, DV, STAGES>;
+  using C = UmmaCfg<DT, DQK, DV, KS, VS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t pad = ((raw_u32 + 1023u) & ~1023u) - raw_u32;
@@ -165,10 +170,11 @@ __global__ void __launch_bounds__(192, 1)
 
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t q_full = bar0;
-  const uint32_t k_full = bar0 + 8;                  // [STAGES]
-  const uint32_t v_full = k_full + 8 * STAGES;       // [STAGES]
-  const uint32_t kv_empty = v_full + 8 * STAGES;     // [STAGES]
-  const uint32_t s_full = kv_empty + 8 * STAGES;     // [2]
+  const uint32_t k_full = bar0 + 8;                  // [KS]
+  const uint32_t k_empty = k_full + 8 * KS;          // [KS]
+  const uint32_t v_full = k_empty + 8 * KS;          // [VS]
+  const uint32_t v_empty = v_full + 8 * VS;          // [VS]
+  const uint32_t s_full = v_empty + 8 * VS;          // [2]
   const uint32_t p_ready = s_full + 16;
   const uint32_t o_ready = p_ready + 8;
   const uint32_t drain = o_ready + 8;
@@ -177,10 +183,13 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < KS; ++s) {
       mbar_init(k_full + 8 * s, 1);
+      mbar_init(k_empty + 8 * s, 1);
+    }
+    for (int s = 0; s < VS; ++s) {
       mbar_init(v_full + 8 * s, 1);
-      mbar_init(kv_empty + 8 * s, 1);
+      mbar_init(v_empty + 8 * s, 1);
     }
     mbar_init(s_full, 1);
     mbar_init(s_full + 8, 1);
@@ -199,7 +208,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  int issued_kv = 0;  // producer: K/V stages issued
+  int issued_k = 0, issued_v = 0;  // producer: K / V blocks issued
 
   if (warp == 0) {
     // -------------------------------------------------------------- producer
@@ -214,24 +223,31 @@ __global__ void __launch_bounds__(192, 1)
       for (int pq = 0; pq < C::NPQ; ++pq)
         tma_load_3d(sbase + C::OFF_Q + pq * C::PANEL, &tmQ, q_full, pq * C::PANEL_ELEMS,
                     kh * group, sq.q0 + q_start, pol_q);
-      for (int j = 0; j < nblk; ++j) {
-        const int st = j % STAGES;
-        if (j >= STAGES && !mbar_wait(kv_empty + 8 * st, ((j / STAGES) - 1) & 1, p.err, abort_flag))
-          break;
-        const uint32_t kdst = sbase + C::OFF_KV + st * C::KV_STAGE;
-        const uint32_t vdst = kdst + C::NPQ * C::PANEL;
-        const int row = sq.k0 + k0 + j * kBlockN;
-        mbar_arrive_expect_tx(k_full + 8 * st, C::NPQ * C::PANEL);
+      // K(0), K(1), V(0), K(2), V(1), ...: K one block ahead of V.
+      for (int j = 0; j <= nblk; ++j) {
+        if (j < nblk) {
+          const int st = j % KS;
+          if (j >= KS && !mbar_wait(k_empty + 8 * st, ((j / KS) - 1) & 1, p.err, abort_flag)) break;
+          const uint32_t dst = sbase + C::OFF_K + st * C::K_STAGE;
+          mbar_arrive_expect_tx(k_full + 8 * st, C::K_STAGE);
 #pragma unroll
-        for (int pk = 0; pk < C::NPQ; ++pk)
-          tma_load_3d(kdst + pk * C::PANEL, &tmK, k_full + 8 * st, pk * C::PANEL_ELEMS, kh, row,
-                      pol_kv);
-        mbar_arrive_expect_tx(v_full + 8 * st, C::NPV * C::PANEL);
+          for (int pk = 0; pk < C::NPQ; ++pk)
+            tma_load_3d(dst + pk * C::PANEL, &tmK, k_full + 8 * st, pk * C::PANEL_ELEMS, kh,
+                        sq.k0 + k0 + j * kBlockN, pol_kv);
+          issued_k = j + 1;
+        }
+        if (j >= 1) {
+          const int jv = j - 1;
+          const int st = jv % VS;
+          if (jv >= VS && !mbar_wait(v_empty + 8 * st, ((jv / VS) - 1) & 1, p.err, abort_flag)) break;
+          const uint32_t dst = sbase + C::OFF_V + st * C::V_STAGE;
+          mbar_arrive_expect_tx(v_full + 8 * st, C::V_STAGE);
 #pragma unroll
-        for (int pv = 0; pv < C::NPV; ++pv)
-          tma_load_3d(vdst + pv * C::PANEL, &tmV, v_full + 8 * st, pv * C::PANEL_ELEMS, kh, row,
-                      pol_kv);
-        issued_kv = j + 1;
+          for (int pv = 0; pv < C::NPV; ++pv)
+            tma_load_3d(dst + pv * C::PANEL, &tmV, v_full + 8 * st, pv * C::PANEL_ELEMS, kh,
+                        sq.k0 + k0 + jv * kBlockN, pol_kv);
+          issued_v = jv + 1;
+        }
       }
     }
   } else if (warp == 1) {
@@ -241,8 +257,8 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t q_addr = sbase + C::OFF_Q;
       const uint32_t p_addr = sbase + C::OFF_P;
       auto issue_s = [&](int j) {
-        const int st = j % STAGES;
-        const uint32_t k_addr = sbase + C::OFF_KV + st * C::KV_STAGE;
+        const int st = j % KS;
+        const uint32_t k_addr = sbase + C::OFF_K + st * C::K_STAGE;
         const uint32_t d = tmem + ((j & 1) ? C::TM_S1 : C::TM_S0);
 #pragma unroll
         for (int ks = 0; ks < C::S_KSTEPS; ++ks) {
@@ -251,6 +267,7 @@ __global__ void __launch_bounds__(192, 1)
                         smem_desc_sw128(k_addr + off, 16, 1024), C::IDESC_S, ks > 0 ? 1u : 0u);
         }
         tc_commit(s_full + 8 * (j & 1));
+        tc_commit(k_empty + 8 * st);
       };
       if (ok) ok = mbar_wait(k_full, 0, p.err, abort_flag);
       if (ok) {
@@ -258,19 +275,19 @@ __global__ void __launch_bounds__(192, 1)
         issue_s(0);
       }
       for (int j = 0; ok && j < nblk; ++j) {
-        const int st = j % STAGES;
+        const int st = j % VS;
         if (j + 1 < nblk) {
-          const int st1 = (j + 1) % STAGES;
-          ok = mbar_wait(k_full + 8 * st1, ((j + 1) / STAGES) & 1, p.err, abort_flag);
+          const int st1 = (j + 1) % KS;
+          ok = mbar_wait(k_full + 8 * st1, ((j + 1) / KS) & 1, p.err, abort_flag);
           if (!ok) break;
           tc_fence_after();
           issue_s(j + 1);
         }
         ok = mbar_wait(p_ready, j & 1, p.err, abort_flag) &&
-             mbar_wait(v_full + 8 * st, (j / STAGES) & 1, p.err, abort_flag);
+             mbar_wait(v_full + 8 * st, (j / VS) & 1, p.err, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t v_addr = sbase + C::OFF_KV + st * C::KV_STAGE + C::NPQ * C::PANEL;
+        const uint32_t v_addr = sbase + C::OFF_V + st * C::V_STAGE;
 #pragma unroll
         for (int ks = 0; ks < C::PV_KSTEPS; ++ks) {
           const uint32_t a_off =
@@ -281,7 +298,7 @@ __global__ void __launch_bounds__(192, 1)
                         (j > 0 || ks > 0) ? 1u : 0u);
         }
         tc_commit(o_ready);
-        tc_commit(kv_empty + 8 * st);
+        tc_commit(v_empty + 8 * st);
       }
       // Let every issued MMA finish before TMEM can be released.
       tc_commit(drain);
@@ -318,8 +335,7 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_after();
         const uint32_t s_addr = tmem + lane_base + ((j & 1) ? C::TM_S1 : C::TM_S0);
         const int kb = k0 + j * kBlockN;
-        tmem_ld64(s_addr, reinterpret_cast<uint32_t*>(s));
-        tmem_ld64(s_addr + 64, reinterpret_cast<uint32_t*>(s) + 64);
+        tmem_ld128(s_addr, reinterpret_cast<uint32_t*>(s));
         // Max of the raw scores (the scale is positive): eight independent
         // chains; keys outside [lo, hi) only exist in boundary blocks.
         float mx[8];
@@ -453,10 +469,13 @@ __global__ void __launch_bounds__(192, 1)
   // ------------------------------------------------------------- teardown
   if (warp == 0 && lane == 0 && *abort_flag) {
     // let issued loads land before the CTA's shared memory is released
-    for (int st = 0; st < STAGES && st < issued_kv; ++st) {
-      const int j_last = st + ((issued_kv - 1 - st) / STAGES) * STAGES;
-      mbar_wait(k_full + 8 * st, (j_last / STAGES) & 1, nullptr, nullptr);
-      mbar_wait(v_full + 8 * st, (j_last / STAGES) & 1, nullptr, nullptr);
+    for (int st = 0; st < KS && st < issued_k; ++st) {
+      const int j_last = st + ((issued_k - 1 - st) / KS) * KS;
+      mbar_wait(k_full + 8 * st, (j_last / KS) & 1, nullptr, nullptr);
+    }
+    for (int st = 0; st < VS && st < issued_v; ++st) {
+      const int j_last = st + ((issued_v - 1 - st) / VS) * VS;
+      mbar_wait(v_full + 8 * st, (j_last / VS) & 1, nullptr, nullptr);
     }
     if (nblk > 0) mbar_wait(q_full, 0, nullptr, nullptr);
   }

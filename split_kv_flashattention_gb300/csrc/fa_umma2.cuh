@@ -1,0 +1,439 @@
+// Tensor-core split kernel with two 128-row query tiles per CTA (256 rows),
+// for prefill-sized tiles.
+//
+// flash-attention PR "[Cute,Fwd,Sm100] Support q_stage=1 for inference",
+// description: a CTA tile of 256 query rows is two parallel M = 128 tensor
+// core pipelines; the review asks whether softmax and MMA overlap.  Here
+// they do: the two tiles (A, B) share every K/V block, and the MMA warp
+// alternates between them so that while one tile's softmax runs, the tensor
+// core works on the other tile:
+//
+//   S_A(0) S_B(0) | PV_A(0) S_A(1) PV_B(0) S_B(1) | PV_A(1) S_A(2) ...
+//
+// Warps (384 threads): 0 TMA producer; 1 TMEM allocator + MMA issuer;
+// 2-3 idle; 4-7 softmax of tile A; 8-11 softmax of tile B (one thread per
+// row = TMEM lane).  TMEM (512 columns): S_A, S_B (128 each), O_A, O_B
+// (d_v each).  P is written back over the S columns it came from as packed
+// 16-bit pairs and the PV MMA reads its A operand from TMEM, so shared memory
+// only holds the two Q tiles and the K/V ring.  Issue order on the MMA warp
+// guarantees PV_A(j) reads P_A(j) before S_A(j+1) overwrites those columns,
+// and the commit that signals S_A(j+1) also covers PV_A(j), so the softmax
+// of block j+1 sees O_A final for block j and can rescale it.
+#pragma once
+
+#include <cuda.h>
+#include <math_constants.h>
+
+#include "fa_common.cuh"
+#include "fa_convert.cuh"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+// D[tmem] (+)= A[tmem] * B[smem desc], 16-bit inputs, fp32 accumulate.
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+template <int DT, int DQK, int DV, int KS, int VS>
+struct Umma2Cfg {
+  static_assert(DT != kE4M3, "two-tile kernel is for 16-bit inputs");
+  static constexpr int ES = 2;
+  static constexpr int PANEL_ELEMS = 64;
+  static constexpr int PANEL = 128 * 128;
+  static constexpr int NPQ = (DQK * ES + 127) / 128;
+  static constexpr int NPV = (DV * ES + 127) / 128;
+  static constexpr int UMMA_K = 16;
+  static constexpr int KSTEPS_PER_PANEL = 4;
+  static constexpr int S_KSTEPS = DQK / UMMA_K;
+  static constexpr int PV_KSTEPS = 128 / UMMA_K;
+  static constexpr int TMEM_COLS = 512;
+  // TMEM columns of tile t's S/P and O
+  __device__ static constexpr int tm_s(int t) { return 128 * t; }
+  __device__ static constexpr int tm_o(int t) { return 256 + DV * t; }
+  static constexpr int OFF_Q = 0;  // tile A panels, then tile B panels
+  static constexpr int K_STAGE = NPQ * PANEL;
+  static constexpr int V_STAGE = NPV * PANEL;
+  static constexpr int OFF_K = OFF_Q + 2 * NPQ * PANEL;
+  static constexpr int OFF_V = OFF_K + KS * K_STAGE;
+  static constexpr int OFF_BAR = OFF_V + VS * V_STAGE;
+  // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], p_ready[2],
+  // o_done[2], drain, turn[2]
+  static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 2 + 2 + 2 + 1 + 2;
+  static constexpr int OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_FLAG = OFF_TMEM_SLOT + 16;
+  static constexpr int SMEM = OFF_FLAG + 16 + 1024;
+  static constexpr int NTHREADS = 384;
+  static constexpr uint32_t IDESC_S = mma_idesc(DT == kBF16 ? 1u : 0u, 128, 128, 0, 0);
+  static constexpr uint32_t IDESC_PV = mma_idesc(DT == kBF16 ? 1u : 0u, 128, DV, 0, 1);
+  static_assert(256 + 2 * DV <= TMEM_COLS, "TMEM columns");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+template <int DT, int DQK, int DV, int KS, int VS>
+__global__ void __launch_bounds__(384, 1)
+    umma2_splitkv_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV) {
+  using C = Umma2Cfg<DT, DQK, DV, KS, VS>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t pad = ((raw_u32 + 1023u) & ~1023u) - raw_u32;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw_u32 + pad;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m_blk = gridDim.x - 1 - blockIdx.x;  // heaviest (latest) tiles first
+  const int b = blockIdx.y / p.h_kv;
+  const int kh = blockIdx.y - b * p.h_kv;
+  const int split = blockIdx.z;
+  const int group = p.group;
+  const int qpt = 128 / group;
+
+  if (timed_out_before(p.err)) return;
+  SeqInfo sq;
+  if (!load_seq(p, b, sq)) {
+    if (threadIdx.x == 0) record_error(p.err, kErrDeviceArg);
+    return;
+  }
+  const int q_start = m_blk * 2 * qpt;
+  if (q_start >= sq.lq) return;
+  const int nq_a = min(qpt, sq.lq - q_start);
+  const int nq_b = max(0, min(qpt, sq.lq - q_start - qpt));
+  const bool has_b = nq_b > 0;
+  int k0, k1;
+  tile_split_range(q_start, q_start + nq_a + nq_b - 1, sq.lq, sq.lk, p.causal, p.window_left,
+                   p.num_splits, split, k0, k1);
+  const int nblk = k1 > k0 ? (k1 - k0 + kBlockN - 1) / kBlockN : 0;
+
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  const uint32_t q_full = bar0;
+  const uint32_t k_full = bar0 + 8;               // [KS]
+  const uint32_t k_empty = k_full + 8 * KS;        // [KS]
+  const uint32_t v_full = k_empty + 8 * KS;        // [VS]
+  const uint32_t v_empty = v_full + 8 * VS;        // [VS]
+  const uint32_t s_full = v_empty + 8 * VS;        // [2]
+  const uint32_t p_ready = s_full + 16;           // [2]
+  const uint32_t o_done = p_ready + 16;           // [2]
+  const uint32_t drain = o_done + 16;
+  const uint32_t turn = drain + 8;                // [2]: softmax ping-pong
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(k_full + 8 * s, 1);
+      mbar_init(k_empty + 8 * s, 1);
+    }
+    for (int s = 0; s < VS; ++s) {
+      mbar_init(v_full + 8 * s, 1);
+      mbar_init(v_empty + 8 * s, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(s_full + 8 * t, 1);
+      mbar_init(p_ready + 8 * t, 128);
+      mbar_init(o_done + 8 * t, 1);
+    }
+    mbar_init(drain, 1);
+    mbar_init(turn, 128);
+    mbar_init(turn + 8, 128);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + C::OFF_TMEM_SLOT, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  int issued_k = 0, issued_v = 0;
+
+  if (warp == 0) {
+    // -------------------------------------------------------------- producer
+    if (lane == 0 && nblk > 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const uint64_t pol_q = l2_policy_evict_first();
+      const uint64_t pol_kv = l2_policy_evict_last();
+      const int ntiles = has_b ? 2 : 1;
+      mbar_arrive_expect_tx(q_full, ntiles * C::NPQ * qpt * group * 128);
+      for (int t = 0; t < ntiles; ++t)
+#pragma unroll
+        for (int pq = 0; pq < C::NPQ; ++pq)
+          tma_load_3d(sbase + C::OFF_Q + (t * C::NPQ + pq) * C::PANEL, &tmQ, q_full,
+                      pq * C::PANEL_ELEMS, kh * group, sq.q0 + q_start + t * qpt, pol_q);
+      // K(0), K(1), V(0), K(2), V(1), ...: K one block ahead of V.
+      for (int j = 0; j <= nblk; ++j) {
+        if (j < nblk) {
+          const int st = j % KS;
+          if (j >= KS && !mbar_wait(k_empty + 8 * st, ((j / KS) - 1) & 1, p.err, abort_flag)) break;
+          const uint32_t dst = sbase + C::OFF_K + st * C::K_STAGE;
+          mbar_arrive_expect_tx(k_full + 8 * st, C::K_STAGE);
+#pragma unroll
+          for (int pk = 0; pk < C::NPQ; ++pk)
+            tma_load_3d(dst + pk * C::PANEL, &tmK, k_full + 8 * st, pk * C::PANEL_ELEMS, kh,
+                        sq.k0 + k0 + j * kBlockN, pol_kv);
+          issued_k = j + 1;
+        }
+        if (j >= 1) {
+          const int jv = j - 1;
+          const int st = jv % VS;
+          if (jv >= VS && !mbar_wait(v_empty + 8 * st, ((jv / VS) - 1) & 1, p.err, abort_flag)) break;
+          const uint32_t dst = sbase + C::OFF_V + st * C::V_STAGE;
+          mbar_arrive_expect_tx(v_full + 8 * st, C::V_STAGE);
+#pragma unroll
+          for (int pv = 0; pv < C::NPV; ++pv)
+            tma_load_3d(dst + pv * C::PANEL, &tmV, v_full + 8 * st, pv * C::PANEL_ELEMS, kh,
+                        sq.k0 + k0 + jv * kBlockN, pol_kv);
+          issued_v = jv + 1;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0 && nblk > 0) {
+      const int ntiles = has_b ? 2 : 1;
+      auto issue_s = [&](int t, int j) {
+        const uint32_t q_addr = sbase + C::OFF_Q + t * C::NPQ * C::PANEL;
+        const uint32_t k_addr = sbase + C::OFF_K + (j % KS) * C::K_STAGE;
+#pragma unroll
+        for (int ks = 0; ks < C::S_KSTEPS; ++ks) {
+          const uint32_t off = (ks / C::KSTEPS_PER_PANEL) * C::PANEL + (ks % C::KSTEPS_PER_PANEL) * 32;
+          tc_mma_f16(tmem + C::tm_s(t), smem_desc_sw128(q_addr + off, 16, 1024),
+                     smem_desc_sw128(k_addr + off, 16, 1024), C::IDESC_S, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(s_full + 8 * t);
+      };
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t v_addr = sbase + C::OFF_V + (j % VS) * C::V_STAGE;
+#pragma unroll
+        for (int ks = 0; ks < C::PV_KSTEPS; ++ks)
+          tc_mma_f16_ts(tmem + C::tm_o(t), tmem + C::tm_s(t) + ks * 8,
+                        smem_desc_sw128(v_addr + ks * C::UMMA_K * 128, C::PANEL, 1024), C::IDESC_PV,
+                        (j > 0 || ks > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(q_full, 0, p.err, abort_flag) && mbar_wait(k_full, 0, p.err, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < ntiles; ++t) issue_s(t, 0);
+        tc_commit(k_empty);  // K(0) is free once both S(0) are done
+      }
+      for (int j = 0; ok && j < nblk; ++j) {
+        for (int t = 0; t < ntiles; ++t) {
+          ok = mbar_wait(p_ready + 8 * t, j & 1, p.err, abort_flag);
+          if (ok && t == 0) ok = mbar_wait(v_full + 8 * (j % VS), (j / VS) & 1, p.err, abort_flag);
+          if (ok && t == 0 && j + 1 < nblk)
+            ok = mbar_wait(k_full + 8 * ((j + 1) % KS), ((j + 1) / KS) & 1, p.err, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, j);
+          if (j + 1 < nblk)
+            issue_s(t, j + 1);
+          else
+            tc_commit(o_done + 8 * t);
+        }
+        if (!ok) break;
+        tc_commit(v_empty + 8 * (j % VS));
+        if (j + 1 < nblk) tc_commit(k_empty + 8 * ((j + 1) % KS));
+      }
+      tc_commit(drain);
+      mbar_wait(drain, 0, nullptr, nullptr);
+    }
+  } else if (warp >= 4) {
+    // ----------------------------------------------------- softmax warps
+    const int t = (warp - 4) >> 2;        // tile 0 (A) or 1 (B)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const int nq = t == 0 ? nq_a : nq_b;
+    const int nrows = nq * group;
+    const bool tile_on = nq > 0;
+    const bool warp_active = quarter * 32 < nrows;
+    const bool row_ok = r < nrows;
+    const int i = q_start + t * qpt + r / group;
+    const int h = kh * group + (r - (r / group) * group);
+    int lo = 0, hi = 0;
+    if (row_ok) {
+      row_key_range(i, sq.lq, sq.lk, p.causal, p.window_left, lo, hi);
+      lo = max(lo, k0);
+      hi = min(hi, k1);
+    }
+    const float sl2 = p.scale * 1.4426950408889634f;
+    float m_run = -CUDART_INF_F, l_run = 0.f;
+    const uint32_t s_addr = tmem + lane_base + C::tm_s(t);
+    const uint32_t o_addr = tmem + lane_base + C::tm_o(t);
+    bool ok = true;
+
+    // The two tiles' softmax blocks strictly alternate, A(0) B(0) A(1) ...:
+    // each runs alone on the SM's issue slots and exp units while the tensor
+    // core works on the other tile.  turn[t] completes when the other tile's
+    // warpgroup has finished the block tile t waits for.
+    for (int j = 0; tile_on && j < nblk; ++j) {
+      if (has_b && (t == 1 || j > 0)) {
+        ok = mbar_wait(turn + 8 * t, (t == 1 ? j : j - 1) & 1, p.err, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+      ok = mbar_wait(s_full + 8 * t, j & 1, p.err, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      if (warp_active) {
+        const int kb = k0 + j * kBlockN;
+        const bool full = kb >= lo && kb + kBlockN <= hi;
+        // pass 1: row max of the raw scores
+        float mx[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx[u] = -CUDART_INF_F;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float s[64];
+          tmem_ld64(s_addr + 64 * hf, reinterpret_cast<uint32_t*>(s));
+          if (full) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              const int key = kb + 64 * hf + c;
+              mx[c & 7] = fmaxf(mx[c & 7], (key >= lo && key < hi) ? s[c] : -CUDART_INF_F);
+            }
+          }
+        }
+        const float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+        const float m_new = (bmax > m_run + 8.f) ? bmax : m_run;  // lazy rescale, 2^8
+        const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
+        const float alpha = m_run == m_new ? 1.f : fast_exp2(m_run - m_use);
+        const bool rescale = j > 0 && m_run != -CUDART_INF_F && alpha != 1.f;
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O holds block j-1's result: the S(j) commit covered PV(j-1).
+#pragma unroll
+          for (int c = 0; c < DV / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(o_addr + 32 * c, o);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+            tmem_st32(o_addr + 32 * c, o);
+          }
+        }
+        // pass 2: probabilities, packed in pairs over the S columns already read
+        float sm[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) sm[u] = 0.f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float s[64];
+          tmem_ld64(s_addr + 64 * hf, reinterpret_cast<uint32_t*>(s));
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            float e0, e1;
+            if (full) {
+              e0 = fast_exp2(fmaf(s[c], sl2, -m_use));
+              e1 = fast_exp2(fmaf(s[c + 1], sl2, -m_use));
+            } else {
+              const int key = kb + 64 * hf + c;
+              e0 = (key >= lo && key < hi) ? fast_exp2(fmaf(s[c], sl2, -m_use)) : 0.f;
+              e1 = (key + 1 >= lo && key + 1 < hi) ? fast_exp2(fmaf(s[c + 1], sl2, -m_use)) : 0.f;
+            }
+            sm[c & 7] += e0;
+            sm[(c + 1) & 7] += e1;
+            pk[c >> 1] = pack2(e0, e1, DT);
+          }
+          tmem_st32(s_addr + 32 * hf, pk);
+        }
+        tmem_st_wait();
+        const float rsum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+        l_run = l_run * alpha + rsum;
+        m_run = m_new;
+      }
+      tc_fence_before();
+      mbar_arrive(p_ready + 8 * t);
+      if (has_b) mbar_arrive(turn + 8 * (1 - t));
+    }
+
+    // ------------------------------------------------------------ epilogue
+    if (tile_on && ok && nblk > 0) {
+      ok = mbar_wait(o_done + 8 * t, 0, p.err, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+    }
+    if (tile_on && warp_active && ok) {
+      float inv = 0.f, lse_v = -CUDART_INF_F;
+      if (row_ok && l_run > 0.f && m_run != -CUDART_INF_F) {
+        inv = 1.f / l_run;
+        lse_v = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+      }
+      const int tok = sq.q0 + i;
+#pragma unroll
+      for (int c = 0; c < DV / 32; ++c) {
+        uint32_t o[32];
+        if (nblk > 0) {
+          tmem_ld32(o_addr + 32 * c, o);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+        if (!row_ok) continue;
+        float f[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(o[e]) * inv;
+        if (p.num_splits == 1) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) +
+                                                ((size_t)tok * p.h_q + h) * (size_t)DV * 2 + c * 64);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(pack2(f[8 * e], f[8 * e + 1], p.out_dtype),
+                                pack2(f[8 * e + 2], f[8 * e + 3], p.out_dtype),
+                                pack2(f[8 * e + 4], f[8 * e + 5], p.out_dtype),
+                                pack2(f[8 * e + 6], f[8 * e + 7], p.out_dtype));
+        } else {
+          const size_t slot = (size_t)b * p.max_seqlen_q + i;
+          float4* dst = reinterpret_cast<float4*>(
+              p.ws_o + (((size_t)split * p.slots + slot) * p.h_q + h) * DV + c * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) dst[e] = make_float4(f[4 * e], f[4 * e + 1], f[4 * e + 2], f[4 * e + 3]);
+        }
+      }
+      if (row_ok) {
+        if (p.num_splits == 1) {
+          if (p.lse != nullptr) p.lse[(size_t)h * p.total_q + tok] = lse_v;
+        } else {
+          const size_t slot = (size_t)b * p.max_seqlen_q + i;
+          p.ws_l[((size_t)split * p.slots + slot) * p.h_q + h] = lse_v;
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------- teardown
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    for (int st = 0; st < KS && st < issued_k; ++st) {
+      const int j_last = st + ((issued_k - 1 - st) / KS) * KS;
+      mbar_wait(k_full + 8 * st, (j_last / KS) & 1, nullptr, nullptr);
+    }
+    for (int st = 0; st < VS && st < issued_v; ++st) {
+      const int j_last = st + ((issued_v - 1 - st) / VS) * VS;
+      mbar_wait(v_full + 8 * st, (j_last / VS) & 1, nullptr, nullptr);
+    }
+    if (nblk > 0) mbar_wait(q_full, 0, nullptr, nullptr);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace fa

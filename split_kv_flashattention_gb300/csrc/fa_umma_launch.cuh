@@ -7,11 +7,11 @@
 
 namespace fa {
 
-template <int DT, int DQK, int DV, int STAGES>
+template <int DT, int DQK, int DV, int KS, int VS>
 cudaError_t launch_umma_one(const FwdParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, dim3 grid, cudaStream_t stream) {
-  using C = UmmaCfg<DT, DQK, DV, STAGES>;
-  auto kern = umma_splitkv_kernel<DT, DQK, DV, STAGES>;
+  using C = UmmaCfg<DT, DQK, DV, KS, VS>;
+  auto kern = umma_splitkv_kernel<DT, DQK, DV, KS, VS>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM);
   if (e != cudaSuccess) return e;
   kern<<<grid, C::NTHREADS, C::SMEM, stream>>>(p, tmQ, tmK, tmV);

@@ -112,7 +112,7 @@ def _call_ex(fa, **kw):
     (dict(q=0), -1),                               # null input
     (dict(in_dtype=2, out_dtype=0, d_qk=192), -1),  # fp8 without descales
     (dict(scale=float("nan")), -1),
-    (dict(flags=3), -1),
+    (dict(flags=3, in_dtype=2, out_dtype=0, d_qk=192, dq=0x9000, dk=0x9000, dv=0x9000), -2),
     (dict(flags=16), -1),                          # unknown flag bit
     (dict(flags=12), -1),                          # partial-only and combine-only
     (dict(num_splits=4, ws=0), -3),                # split without workspace

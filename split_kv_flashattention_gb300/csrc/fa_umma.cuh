@@ -51,7 +51,10 @@ struct UmmaCfg {
   static constexpr int PANEL = 128 * 128;                  // 128 rows x 128 bytes
   static constexpr int NPQ = (DQK * ES + 127) / 128;       // panels of Q / K
   static constexpr int NPV = (DV * ES + 127) / 128;        // panels of V
-  static constexpr int NPP = ES;                           // panels of P (128 keys)
+  // 16-bit P stays in TMEM (over the S columns it came from) as the PV
+  // MMA's A operand; e4m3 P goes through shared memory.
+  static constexpr bool P_TMEM = DT != kE4M3;
+  static constexpr int NPP = P_TMEM ? 0 : ES;              // smem panels of P
   static constexpr int UMMA_K = 32 / ES;                   // K elements per MMA
   static constexpr int KSTEPS_PER_PANEL = PANEL_ELEMS / UMMA_K;
   static constexpr int S_KSTEPS = (DQK + UMMA_K - 1) / UMMA_K;
@@ -290,12 +293,18 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t v_addr = sbase + C::OFF_V + st * C::V_STAGE;
 #pragma unroll
         for (int ks = 0; ks < C::PV_KSTEPS; ++ks) {
-          const uint32_t a_off =
-              (ks / C::KSTEPS_PER_PANEL) * C::PANEL + (ks % C::KSTEPS_PER_PANEL) * 32;
           const uint32_t b_off = ks * C::UMMA_K * 128;
-          mma_issue<DT>(tmem + C::TM_O, smem_desc_sw128(p_addr + a_off, 16, 1024),
-                        smem_desc_sw128(v_addr + b_off, C::PANEL, 1024), C::IDESC_PV,
-                        (j > 0 || ks > 0) ? 1u : 0u);
+          const uint64_t v_desc = smem_desc_sw128(v_addr + b_off, C::PANEL, 1024);
+          const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
+          if constexpr (C::P_TMEM) {
+            tc_mma_f16_ts(tmem + C::TM_O, tmem + ((j & 1) ? C::TM_S1 : C::TM_S0) + ks * 8, v_desc,
+                          C::IDESC_PV, acc);
+          } else {
+            const uint32_t a_off =
+                (ks / C::KSTEPS_PER_PANEL) * C::PANEL + (ks % C::KSTEPS_PER_PANEL) * 32;
+            mma_issue<DT>(tmem + C::TM_O, smem_desc_sw128(p_addr + a_off, 16, 1024), v_desc,
+                          C::IDESC_PV, acc);
+          }
         }
         tc_commit(o_ready);
         tc_commit(v_empty + 8 * st);
@@ -395,16 +404,30 @@ __global__ void __launch_bounds__(192, 1)
         }
         l_run = l_run * alpha + rsum;
         m_run = m_new;
-        // P row, 128B-swizzled K-major: 16-byte chunk c of panel pp at
-        // position c ^ (r % 8).
-        constexpr int EPC = 16 / C::ES;  // P elements per 16-byte chunk
+        if constexpr (C::P_TMEM) {
+          // P over the first 64 columns of this block's S buffer (already read):
+          // column c holds keys 2c (low half) and 2c+1.
+          const uint32_t p_addr_t = tmem + lane_base + ((j & 1) ? C::TM_S1 : C::TM_S0);
 #pragma unroll
-        for (int c = 0; c < 128 / EPC; ++c) {
-          const int pp = c / 8, cc = c % 8;
-          const uint4 w = pack_p16<DT>(s + c * EPC);
-          *reinterpret_cast<uint4*>(p_row + pp * C::PANEL + ((cc ^ (r & 7)) << 4)) = w;
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) pk[c] = pack2(s[64 * h2 + 2 * c], s[64 * h2 + 2 * c + 1], DT);
+            tmem_st32(p_addr_t + 32 * h2, pk);
+          }
+          tmem_st_wait();
+        } else {
+          // P row, 128B-swizzled K-major: 16-byte chunk c of panel pp at
+          // position c ^ (r % 8).
+          constexpr int EPC = 16 / C::ES;  // P elements per 16-byte chunk
+#pragma unroll
+          for (int c = 0; c < 128 / EPC; ++c) {
+            const int pp = c / 8, cc = c % 8;
+            const uint4 w = pack_p16<DT>(s + c * EPC);
+            *reinterpret_cast<uint4*>(p_row + pp * C::PANEL + ((cc ^ (r & 7)) << 4)) = w;
+          }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
       }
       tc_fence_before();
       mbar_arrive(p_ready);

@@ -30,15 +30,9 @@
 
 namespace fa {
 
-// D[tmem] (+)= A[tmem] * B[smem desc], 16-bit inputs, fp32 accumulate.
-__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
+// Whether the two softmax warpgroups strictly alternate (measured slower on
+// GB300: each tile's softmax then runs on one warp per SM sub-partition).
+constexpr bool kPingPong = false;
 
 template <int DT, int DQK, int DV, int KS, int VS>
 struct Umma2Cfg {
@@ -280,7 +274,7 @@ __global__ void __launch_bounds__(384, 1)
     // core works on the other tile.  turn[t] completes when the other tile's
     // warpgroup has finished the block tile t waits for.
     for (int j = 0; tile_on && j < nblk; ++j) {
-      if (has_b && (t == 1 || j > 0)) {
+      if (kPingPong && has_b && (t == 1 || j > 0)) {
         ok = mbar_wait(turn + 8 * t, (t == 1 ? j : j - 1) & 1, p.err, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) break;
       }
@@ -359,7 +353,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       tc_fence_before();
       mbar_arrive(p_ready + 8 * t);
-      if (has_b) mbar_arrive(turn + 8 * (1 - t));
+      if (kPingPong && has_b) mbar_arrive(turn + 8 * (1 - t));
     }
 
     // ------------------------------------------------------------ epilogue

@@ -182,15 +182,27 @@ cudaError_t launch_umma(int dtype, int d_qk, int d_v, const FwdParams& p, const 
   return cudaErrorInvalidValue;
 }
 
+// The combine is launched with programmatic stream serialisation so its
+// launch overlaps the tail of the partial kernel; it waits for the partial
+// grid's writes with griddepcontrol.wait.
 cudaError_t launch_combine(const FwdParams& p, cudaStream_t stream) {
   const long long warps = (long long)p.slots * p.h_q;
   const unsigned blocks = (unsigned)((warps + 3) / 4);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   switch (p.d_v) {
-    case 64: combine_kernel<64><<<blocks, 128, 0, stream>>>(p); break;
-    case 128: combine_kernel<128><<<blocks, 128, 0, stream>>>(p); break;
-    default: return cudaErrorInvalidValue;
+    case 64: return cudaLaunchKernelEx(&cfg, combine_kernel<64>, p);
+    case 128: return cudaLaunchKernelEx(&cfg, combine_kernel<128>, p);
   }
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_split_ranges(const int* cu_q, const int* cu_k, int batch, int max_seqlen_q,

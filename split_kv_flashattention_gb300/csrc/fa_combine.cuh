@@ -21,6 +21,9 @@ namespace fa {
 template <int DV>
 __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ FwdParams p) {
   constexpr int DPL = DV / 32;
+  // Launched as a programmatic dependent of the partial kernel: wait for its
+  // partials before reading them.
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (gw >= (long long)p.slots * p.h_q) return;

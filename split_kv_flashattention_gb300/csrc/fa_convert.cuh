@@ -69,6 +69,45 @@ __device__ __forceinline__ void words_to_float(const uint32_t* w, float* f) {
   for (int i = 0; i < NWORDS; ++i) word_to_float<DT>(w[i], f + i * PerWord<DT>::n);
 }
 
+// ----------------------------------------------------------- packed fp32x2
+// Two fp32 values in one 64-bit register pair; sm_100-class SMs execute
+// fma/mul on such pairs as one instruction (twice the FP32 rate per issue).
+using f32x2 = unsigned long long;
+
+__device__ __forceinline__ f32x2 f2_make(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ float2 f2_split(f32x2 v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+
+// a * b + c on both halves
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// One 32-bit word of packed elements -> pairs (1 pair for 16-bit, 2 for e4m3).
+template <int DT>
+__device__ __forceinline__ void word_to_f2(uint32_t w, f32x2* f) {
+  float t[4];
+  word_to_float<DT>(w, t);
+  f[0] = f2_make(t[0], t[1]);
+  if constexpr (DT == kE4M3) f[1] = f2_make(t[2], t[3]);
+}
+
 // Two floats -> one packed 16-bit pair for the output type (round to nearest).
 __device__ __forceinline__ uint32_t pack2(float a, float b, int out_dtype) {
   if (out_dtype == kFP16) {

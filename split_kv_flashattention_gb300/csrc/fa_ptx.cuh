@@ -192,6 +192,18 @@ __device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, 
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc], e4m3 inputs, fp32 accumulate.  A holds
+// four e4m3 K elements per 32-bit column (lowest K index in the lowest
+// byte); one K=32 step spans 8 columns.
+__device__ __forceinline__ void tc_mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Same for 8-bit float inputs (e4m3 x e4m3 -> fp32).
 __device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
@@ -268,6 +280,19 @@ __host__ __device__ constexpr uint32_t mma_idesc(uint32_t ab_format, uint32_t m,
   return (1u << 4) | (ab_format << 7) | (ab_format << 10) | (a_mn_major << 15) |
          (b_mn_major << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
+
+// ------------------------------------------------ programmatic dependent launch
+
+// Lets a kernel launched after this one with programmatic stream
+// serialisation start launching (its griddepcontrol.wait still waits for
+// this grid to finish and its writes to be visible).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the grids this one depends on have completed and flushed.
+// Returns at once when the kernel was not launched as a dependent.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ----------------------------------------------------------- math helpers
 

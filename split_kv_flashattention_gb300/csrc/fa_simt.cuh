@@ -157,14 +157,14 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     float qscale = p.scale * 1.4426950408889634f;
     if (DT == kE4M3) qscale *= __ldg(p.descale_q) * __ldg(p.descale_k);
 
-    float qf[RT][C::QR];
+    f32x2 qf[RT][C::QR / 2];  // query values of this lane's columns, in pairs
     int lo_r[RT], hi_r[RT];
 #pragma unroll
     for (int r = 0; r < RT; ++r) {
       lo_r[r] = 0;
       hi_r[r] = 0;
 #pragma unroll
-      for (int e = 0; e < C::QR; ++e) qf[r][e] = 0.f;
+      for (int e = 0; e < C::QR / 2; ++e) qf[r][e] = 0ull;
       if (r < nrows) {
         const int R = r0 + r;
         const int i = R / p.group;
@@ -183,7 +183,8 @@ __global__ void __launch_bounds__((NW + 1) * 32)
             float f[C::EPC];
             words_to_float<DT, 4>(w, f);
 #pragma unroll
-            for (int e = 0; e < C::EPC; ++e) qf[r][t * C::EPC + e] = f[e] * qscale;
+            for (int e = 0; e < C::EPC; e += 2)
+              qf[r][(t * C::EPC + e) / 2] = f2_make(f[e] * qscale, f[e + 1] * qscale);
           }
         }
         int lo, hi;
@@ -193,13 +194,14 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       }
     }
 
-    float m_run[RT], l_run[RT], acc[RT][C::DPL];
+    float m_run[RT], l_run[RT];
+    f32x2 acc[RT][C::DPL / 2];  // this lane's output columns, in pairs
 #pragma unroll
     for (int r = 0; r < RT; ++r) {
       m_run[r] = -CUDART_INF_F;
       l_run[r] = 0.f;
 #pragma unroll
-      for (int e = 0; e < C::DPL; ++e) acc[r][e] = 0.f;
+      for (int e = 0; e < C::DPL / 2; ++e) acc[r][e] = 0ull;
     }
     float* ps = reinterpret_cast<float*>(smem + C::OFF_PS) + warp * RT * C::KC;
 
@@ -221,25 +223,30 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
         const int krow = it * 8 + kk;
-        float d[RT];
+        f32x2 d2[RT];
 #pragma unroll
-        for (int r = 0; r < RT; ++r) d[r] = 0.f;
+        for (int r = 0; r < RT; ++r) d2[r] = 0ull;
 #pragma unroll
         for (int t = 0; t < C::CPL; ++t) {
           const int pk = t >> 1, half = t & 1;
           const int pc = sub + 4 * ((half + kk) & 1);
           uint32_t w[4];
           lds_words<16>(kbase + pk * C::PANEL + krow * 128 + pc * 16, w);
-          float kv[C::EPC];
-          words_to_float<DT, 4>(w, kv);
+          f32x2 kv[C::EPC / 2];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) word_to_f2<DT>(w[u], kv + u * (C::EPC / 8));
 #pragma unroll
           for (int r = 0; r < RT; ++r)
 #pragma unroll
-            for (int e = 0; e < C::EPC; ++e) d[r] = fmaf(qf[r][t * C::EPC + e], kv[e], d[r]);
+            for (int e = 0; e < C::EPC / 2; ++e)
+              d2[r] = f2_fma(qf[r][(t * C::EPC) / 2 + e], kv[e], d2[r]);
         }
         const int j = key_base + krow;
+        float d[RT];
 #pragma unroll
         for (int r = 0; r < RT; ++r) {
+          const float2 dd = f2_split(d2[r]);
+          d[r] = dd.x + dd.y;
           d[r] += __shfl_xor_sync(0xffffffffu, d[r], 1);
           d[r] += __shfl_xor_sync(0xffffffffu, d[r], 2);
           sc[r][it] = (j >= lo_r[r] && j < hi_r[r]) ? d[r] : -CUDART_INF_F;
@@ -262,8 +269,9 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         }
         m_run[r] = m_new;
         l_run[r] = l_run[r] * alpha + (sub == 0 ? (pv[0] + pv[1]) + (pv[2] + pv[3]) : 0.f);
+        const f32x2 a2 = f2_make(alpha, alpha);
 #pragma unroll
-        for (int e = 0; e < C::DPL; ++e) acc[r][e] *= alpha;
+        for (int e = 0; e < C::DPL / 2; ++e) acc[r][e] = f2_mul(acc[r][e], a2);
         if (sub == 0) {
 #pragma unroll
           for (int it = 0; it < 4; ++it) ps[r * C::KC + it * 8 + kk] = pv[it];
@@ -282,21 +290,22 @@ __global__ void __launch_bounds__((NW + 1) * 32)
           uint32_t w[(C::BPL + 3) / 4];
           lds_words<C::BPL>(vbase + v_panel * C::PANEL + vrow * 128 + ((v_lc ^ (vrow & 7)) << 4) + v_off,
                             w);
-          float vv[C::DPL];
+          f32x2 vv[C::DPL / 2];
           if constexpr (C::BPL >= 4) {
-            words_to_float<DT, C::BPL / 4>(w, vv);
+#pragma unroll
+            for (int u2 = 0; u2 < C::BPL / 4; ++u2) word_to_f2<DT>(w[u2], vv + u2 * (C::DPL / 2) / (C::BPL / 4));
           } else {
             // 2 bytes = two e4m3 values
             __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[0]), __NV_E4M3);
-            float2 f2 = __half22float2(*reinterpret_cast<__half2*>(&h2));
-            vv[0] = f2.x;
-            vv[1] = f2.y;
+            float2 fv = __half22float2(*reinterpret_cast<__half2*>(&h2));
+            vv[0] = f2_make(fv.x, fv.y);
           }
 #pragma unroll
           for (int r = 0; r < RT; ++r) {
             const float pw = u == 0 ? pr[r].x : u == 1 ? pr[r].y : u == 2 ? pr[r].z : pr[r].w;
+            const f32x2 pw2 = f2_make(pw, pw);
 #pragma unroll
-            for (int e = 0; e < C::DPL; ++e) acc[r][e] = fmaf(pw, vv[e], acc[r][e]);
+            for (int e = 0; e < C::DPL / 2; ++e) acc[r][e] = f2_fma(pw2, vv[e], acc[r][e]);
           }
         }
       }
@@ -316,10 +325,15 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         dst[1] = l;
       }
 #pragma unroll
-      for (int e = 0; e < C::DPL; ++e) dst[2 + lane * C::DPL + e] = acc[r][e];
+      for (int e = 0; e < C::DPL / 2; ++e) {
+        const float2 a = f2_split(acc[r][e]);
+        dst[2 + lane * C::DPL + 2 * e] = a.x;
+        dst[2 + lane * C::DPL + 2 * e + 1] = a.y;
+      }
     }
   }
   __syncthreads();
+  pdl_launch_dependents();
 
   // ------------------------------------------------------------ epilogue
   if (warp < nrows) {

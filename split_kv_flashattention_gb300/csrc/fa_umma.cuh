@@ -51,10 +51,10 @@ struct UmmaCfg {
   static constexpr int PANEL = 128 * 128;                  // 128 rows x 128 bytes
   static constexpr int NPQ = (DQK * ES + 127) / 128;       // panels of Q / K
   static constexpr int NPV = (DV * ES + 127) / 128;        // panels of V
-  // 16-bit P stays in TMEM (over the S columns it came from) as the PV
-  // MMA's A operand; e4m3 P goes through shared memory.
-  static constexpr bool P_TMEM = DT != kE4M3;
-  static constexpr int NPP = P_TMEM ? 0 : ES;              // smem panels of P
+  // P stays in TMEM (over the S columns it came from) as the PV MMA's A
+  // operand: 16-bit P two per column, e4m3 P four per column.
+  static constexpr bool P_TMEM = true;
+  static constexpr int NPP = 0;                            // smem panels of P
   static constexpr int UMMA_K = 32 / ES;                   // K elements per MMA
   static constexpr int KSTEPS_PER_PANEL = PANEL_ELEMS / UMMA_K;
   static constexpr int S_KSTEPS = (DQK + UMMA_K - 1) / UMMA_K;
@@ -297,8 +297,11 @@ __global__ void __launch_bounds__(192, 1)
           const uint64_t v_desc = smem_desc_sw128(v_addr + b_off, C::PANEL, 1024);
           const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
           if constexpr (C::P_TMEM) {
-            tc_mma_f16_ts(tmem + C::TM_O, tmem + ((j & 1) ? C::TM_S1 : C::TM_S0) + ks * 8, v_desc,
-                          C::IDESC_PV, acc);
+            const uint32_t a_t = tmem + ((j & 1) ? C::TM_S1 : C::TM_S0) + ks * 8;
+            if constexpr (DT == kE4M3)
+              tc_mma_f8_ts(tmem + C::TM_O, a_t, v_desc, C::IDESC_PV, acc);
+            else
+              tc_mma_f16_ts(tmem + C::TM_O, a_t, v_desc, C::IDESC_PV, acc);
           } else {
             const uint32_t a_off =
                 (ks / C::KSTEPS_PER_PANEL) * C::PANEL + (ks % C::KSTEPS_PER_PANEL) * 32;
@@ -370,16 +373,20 @@ __global__ void __launch_bounds__(192, 1)
         // alpha rescales what was accumulated so far; a row that has seen no
         // key yet holds O = 0 and l = 0, so it needs no rescale.
         alpha = m_run == m_new ? 1.f : fast_exp2(m_run - m_use);
+        // e4m3 P is produced pre-scaled by kP8Scale = 2^4 (offset in the
+        // exponent); the row sum is scaled back exactly.
+        const float e_off = DT == kE4M3 ? m_use - 4.f : m_use;
         float sm[8];
 #pragma unroll
         for (int t = 0; t < 8; ++t) sm[t] = 0.f;
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
-          const float e = fast_exp2(fmaf(s[c], sl2, -m_use));  // masked: exp2(-inf) = 0
+          const float e = fast_exp2(fmaf(s[c], sl2, -e_off));  // masked: exp2(-inf) = 0
           s[c] = e;
           sm[c & 7] += e;
         }
         rsum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+        if (DT == kE4M3) rsum *= 1.f / kP8Scale;
       }
       // PV of the previous block must be done before O is rescaled and the
       // P buffer is overwritten (the exponentials above overlap it).
@@ -408,12 +415,26 @@ __global__ void __launch_bounds__(192, 1)
           // P over the first 64 columns of this block's S buffer (already read):
           // column c holds keys 2c (low half) and 2c+1.
           const uint32_t p_addr_t = tmem + lane_base + ((j & 1) ? C::TM_S1 : C::TM_S0);
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
+          if constexpr (DT == kE4M3) {
+            // e4m3: probabilities were produced pre-scaled by kP8Scale
             uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) pk[c] = pack2(s[64 * h2 + 2 * c], s[64 * h2 + 2 * c + 1], DT);
-            tmem_st32(p_addr_t + 32 * h2, pk);
+            for (int c = 0; c < 32; ++c) {
+              const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                  make_float2(s[4 * c], s[4 * c + 1]), __NV_SATFINITE, __NV_E4M3);
+              const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                  make_float2(s[4 * c + 2], s[4 * c + 3]), __NV_SATFINITE, __NV_E4M3);
+              pk[c] = (uint32_t)lo | ((uint32_t)hi << 16);
+            }
+            tmem_st32(p_addr_t, pk);
+          } else {
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              uint32_t pk[32];
+#pragma unroll
+              for (int c = 0; c < 32; ++c) pk[c] = pack2(s[64 * h2 + 2 * c], s[64 * h2 + 2 * c + 1], DT);
+              tmem_st32(p_addr_t + 32 * h2, pk);
+            }
           }
           tmem_st_wait();
         } else {
@@ -434,6 +455,7 @@ __global__ void __launch_bounds__(192, 1)
     }
 
     // ------------------------------------------------------------ epilogue
+    pdl_launch_dependents();
     if (ok && nblk > 0) {
       ok = mbar_wait(o_ready, (nblk - 1) & 1, p.err, abort_flag);
       ok = __all_sync(0xffffffffu, ok);

@@ -357,6 +357,7 @@ __global__ void __launch_bounds__(384, 1)
     }
 
     // ------------------------------------------------------------ epilogue
+    pdl_launch_dependents();
     if (tile_on && ok && nblk > 0) {
       ok = mbar_wait(o_done + 8 * t, 0, p.err, abort_flag);
       ok = __all_sync(0xffffffffu, ok);

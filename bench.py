@@ -137,6 +137,23 @@ def prefill_secondary(fa, dev, steps, warmup):
     return res
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of every rank's value (the step time the job waited for);
+    plain value at world size 1.  Works with the nccl and gloo backends."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job rate: every rank processes its own replica of the workload
+    (weak scaling), so the units of all ranks are divided by the slowest
+    rank's step time.  Returned per second, in units / 1e12."""
+    return world * units_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -469,19 +486,16 @@ def main():
     if err != 0:
         raise RuntimeError(f"device error {fa.fa_status_string(err)}")
 
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
     metric_bytes, partial_bytes = byte_counts(inp, ns)
     work_flops = flops(inp, causal)
     if kind == "tensor":
         unit = "TFLOPS"
-        value = world * work_flops / (ms_per_step * 1e-3) / 1e12
+        value = job_throughput(work_flops, world, ms_per_step)
     else:
         unit = "TB/s"
-        value = world * metric_bytes / (ms_per_step * 1e-3) / 1e12
+        value = job_throughput(metric_bytes, world, ms_per_step)
 
     # ---- end to end through the public call with host buffers
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
@@ -512,11 +526,8 @@ def main():
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    te = torch.tensor([e0.elapsed_time(e1) / e2e_steps], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
-    e2e_ms = float(te.item())
-    e2e_value = world * (work_flops if kind == "tensor" else metric_bytes) / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    e2e_value = job_throughput(work_flops if kind == "tensor" else metric_bytes, world, e2e_ms)
 
     secondary = None
     if kind == "hbm" and world == 1 and not args.no_prefill:

@@ -353,17 +353,18 @@ __global__ void __launch_bounds__(192, 1)
         float mx[8];
 #pragma unroll
         for (int t = 0; t < 8; ++t) mx[t] = -CUDART_INF_F;
-        if (kb >= lo && kb + kBlockN <= hi) {
-#pragma unroll
-          for (int c = 0; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-        } else {
+        if (!(kb >= lo && kb + kBlockN <= hi)) {
 #pragma unroll
           for (int c = 0; c < 128; ++c) {
             const int key = kb + c;
             s[c] = (key >= lo && key < hi) ? s[c] : -CUDART_INF_F;
-            mx[c & 7] = fmaxf(mx[c & 7], s[c]);
           }
         }
+        // three-input max: 8 chains over 16 values each
+#pragma unroll
+        for (int c = 0; c < 128; c += 16)
+#pragma unroll
+          for (int t = 0; t < 8; ++t) mx[t] = fmax3(mx[t], s[c + t], s[c + 8 + t]);
         const float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
         // Lazy rescale: keep the max in use unless the block's max exceeds
@@ -376,16 +377,22 @@ __global__ void __launch_bounds__(192, 1)
         // e4m3 P is produced pre-scaled by kP8Scale = 2^4 (offset in the
         // exponent); the row sum is scaled back exactly.
         const float e_off = DT == kE4M3 ? m_use - 4.f : m_use;
-        float sm[8];
+        // exponent arguments and row sums on packed fp32 pairs
+        const f32x2 sl2x2 = f2_make(sl2, sl2);
+        const f32x2 noff = f2_make(-e_off, -e_off);
+        f32x2 sm[4];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) sm[t] = 0.f;
+        for (int t = 0; t < 4; ++t) sm[t] = 0ull;
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const float e = fast_exp2(fmaf(s[c], sl2, -e_off));  // masked: exp2(-inf) = 0
-          s[c] = e;
-          sm[c & 7] += e;
+        for (int c = 0; c < 128; c += 2) {
+          const float2 x = f2_split(f2_fma(f2_make(s[c], s[c + 1]), sl2x2, noff));
+          const float e0 = fast_exp2(x.x), e1 = fast_exp2(x.y);  // masked: exp2(-inf) = 0
+          s[c] = e0;
+          s[c + 1] = e1;
+          sm[(c >> 1) & 3] = f2_add(sm[(c >> 1) & 3], f2_make(e0, e1));
         }
-        rsum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+        const float2 r01 = f2_split(f2_add(f2_add(sm[0], sm[1]), f2_add(sm[2], sm[3])));
+        rsum = r01.x + r01.y;
         if (DT == kE4M3) rsum *= 1.f / kP8Scale;
       }
       // PV of the previous block must be done before O is rescaled and the

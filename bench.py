@@ -409,6 +409,8 @@ def main():
     if args.kernel == "auto":
         if rows <= simt_rows:
             kern_tag = "simt_splitkv"
+        elif rows > 128 and inp.dtype != "e4m3":
+            kern_tag = "umma2_splitkv"
         else:
             kern_tag = "umma_splitkv"
     else:

@@ -120,9 +120,9 @@ typedef enum {
  *                 (per-tensor dequantisation factors), ignored otherwise.
  *  flags          FA_KERNEL_* selection, optionally OR FA_RUN_*_ONLY.  AUTO
  *                 picks the CUDA-core kernel for up to 4 rows (queries x
- *                 group) per KV head (2 for e4m3 with d_qk=192) and the
- *                 one-tile tcgen05 kernel beyond; the two-tile kernel is
- *                 only used when requested.
+ *                 group) per KV head (2 for e4m3 with d_qk=192), the
+ *                 one-tile tcgen05 kernel up to 128 rows and for e4m3, and
+ *                 the two-tile tcgen05 kernel beyond 128 rows.
  *  stream         cudaStream_t.
  * Returns FA_OK or a negative fa_status.
  */

@@ -382,10 +382,10 @@ int fa_fwd_splitkv_ex(const void* q, const void* k, const void* v, const int* cu
   const int rows = max_seqlen_q * p.group;
   const int rt_max = simt_max_rows(in_dtype, d_qk, d_v);
   const bool auto_tc = kernel_sel == FA_KERNEL_AUTO && rows > rt_max;
-  // The one-tile kernel is the faster tensor-core path on GB300 for every
-  // measured shape, so AUTO uses it; the two-tile kernel is selected
-  // explicitly.
-  const bool use_umma2 = kernel_sel == FA_KERNEL_UMMA2;
+  // More than one 128-row tile per KV head with 16-bit inputs: two tiles per
+  // CTA share each K/V block and overlap their softmax with the other tile's
+  // MMAs.  Otherwise one tile per CTA.
+  const bool use_umma2 = kernel_sel == FA_KERNEL_UMMA2 || (auto_tc && rows > 128 && in_dtype != kE4M3);
   const bool use_umma = !use_umma2 && (kernel_sel == FA_KERNEL_UMMA || auto_tc);
   if ((unsigned)(batch * h_kv) > 65535u) return FA_ERR_UNSUPPORTED;
   if (run_partial) {

@@ -281,6 +281,19 @@ __host__ __device__ constexpr uint32_t mma_idesc(uint32_t ab_format, uint32_t m,
          (b_mn_major << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
+// ------------------------------------------------------ register budgets
+// Per-warpgroup register reallocation.  Both must be executed by all 128
+// threads of a warpgroup; increases draw only on registers released by
+// decreases within the same CTA's launch allocation.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------ programmatic dependent launch
 
 // Lets a kernel launched after this one with programmatic stream

@@ -10,9 +10,11 @@
 //
 //   S_A(0) S_B(0) | PV_A(0) S_A(1) PV_B(0) S_B(1) | PV_A(1) S_A(2) ...
 //
-// Warps (384 threads): 0 TMA producer; 1 TMEM allocator + MMA issuer;
-// 2-3 idle; 4-7 softmax of tile A; 8-11 softmax of tile B (one thread per
-// row = TMEM lane).  TMEM (512 columns): S_A, S_B (128 each), O_A, O_B
+// Warps (384 threads, three warpgroups): 0 TMA producer; 1 TMEM allocator +
+// MMA issuer; 2-3 idle; 4-7 softmax of tile A; 8-11 softmax of tile B (one
+// thread per row = TMEM lane; warp w reads TMEM lanes 32*(w%4) ..
+// 32*(w%4)+31).  setmaxnreg moves registers from the first warpgroup to the
+// softmax warpgroups, which keep a whole 128-column S row in registers.  TMEM (512 columns): S_A, S_B (128 each), O_A, O_B
 // (d_v each).  P is written back over the S columns it came from as packed
 // 16-bit pairs and the PV MMA reads its A operand from TMEM, so shared memory
 // only holds the two Q tiles and the K/V ring.  Issue order on the MMA warp
@@ -31,7 +33,8 @@
 namespace fa {
 
 // Whether the two softmax warpgroups strictly alternate (measured slower on
-// GB300: each tile's softmax then runs on one warp per SM sub-partition).
+// GB300 than letting both run: each tile's softmax then has only one warp
+// per SM sub-partition to hide latency with).
 constexpr bool kPingPong = false;
 
 template <int DT, int DQK, int DV, int KS, int VS>
@@ -63,6 +66,11 @@ struct Umma2Cfg {
   static constexpr int OFF_FLAG = OFF_TMEM_SLOT + 16;
   static constexpr int SMEM = OFF_FLAG + 16 + 1024;
   static constexpr int NTHREADS = 384;
+  // Register split (launch: 384 x 168 = 64512): the TMA/MMA warpgroup gives
+  // registers to the two softmax warpgroups, 128*56 + 256*224 = 64512.
+  static constexpr int REGS_CTRL = 56;
+  static constexpr int REGS_SOFTMAX = 224;
+  static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX <= 384 * 168, "register split");
   static constexpr uint32_t IDESC_S = mma_idesc(DT == kBF16 ? 1u : 0u, 128, 128, 0, 0);
   static constexpr uint32_t IDESC_PV = mma_idesc(DT == kBF16 ? 1u : 0u, 128, DV, 0, 1);
   static_assert(256 + 2 * DV <= TMEM_COLS, "TMEM columns");
@@ -149,7 +157,10 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
+  // The two register budgets never meet again: each side runs its own
+  // teardown (CTA barrier, then the TMEM release on the MMA warp).
+  if (warp < 4) {
+    regs_dec<C::REGS_CTRL>();
   int issued_k = 0, issued_v = 0;
 
   if (warp == 0) {
@@ -244,9 +255,29 @@ __global__ void __launch_bounds__(384, 1)
       tc_commit(drain);
       mbar_wait(drain, 0, nullptr, nullptr);
     }
-  } else if (warp >= 4) {
+  }
+  // ----------------------------------------------------- teardown (TMA/MMA side)
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    for (int st = 0; st < KS && st < issued_k; ++st) {
+      const int j_last = st + ((issued_k - 1 - st) / KS) * KS;
+      mbar_wait(k_full + 8 * st, (j_last / KS) & 1, nullptr, nullptr);
+    }
+    for (int st = 0; st < VS && st < issued_v; ++st) {
+      const int j_last = st + ((issued_v - 1 - st) / VS) * VS;
+      mbar_wait(v_full + 8 * st, (j_last / VS) & 1, nullptr, nullptr);
+    }
+    if (nblk > 0) mbar_wait(q_full, 0, nullptr, nullptr);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  } else {
+    regs_inc<C::REGS_SOFTMAX>();
     // ----------------------------------------------------- softmax warps
-    const int t = (warp - 4) >> 2;        // tile 0 (A) or 1 (B)
+    const int t = (warp - 4) >> 2;        // tile 0 (A): warps 4-7, tile 1 (B): warps 8-11
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -269,10 +300,6 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t o_addr = tmem + lane_base + C::tm_o(t);
     bool ok = true;
 
-    // The two tiles' softmax blocks strictly alternate, A(0) B(0) A(1) ...:
-    // each runs alone on the SM's issue slots and exp units while the tensor
-    // core works on the other tile.  turn[t] completes when the other tile's
-    // warpgroup has finished the block tile t waits for.
     for (int j = 0; tile_on && j < nblk; ++j) {
       if (kPingPong && has_b && (t == 1 || j > 0)) {
         ok = mbar_wait(turn + 8 * t, (t == 1 ? j : j - 1) & 1, p.err, abort_flag);
@@ -283,26 +310,22 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       if (warp_active) {
         const int kb = k0 + j * kBlockN;
-        const bool full = kb >= lo && kb + kBlockN <= hi;
-        // pass 1: row max of the raw scores
+        float s[128];
+        tmem_ld128(s_addr, reinterpret_cast<uint32_t*>(s));
+        if (!(kb >= lo && kb + kBlockN <= hi)) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const int key = kb + c;
+            s[c] = (key >= lo && key < hi) ? s[c] : -CUDART_INF_F;
+          }
+        }
         float mx[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) mx[u] = -CUDART_INF_F;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          float s[64];
-          tmem_ld64(s_addr + 64 * hf, reinterpret_cast<uint32_t*>(s));
-          if (full) {
+        for (int c = 0; c < 128; c += 16)
 #pragma unroll
-            for (int c = 0; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 64; ++c) {
-              const int key = kb + 64 * hf + c;
-              mx[c & 7] = fmaxf(mx[c & 7], (key >= lo && key < hi) ? s[c] : -CUDART_INF_F);
-            }
-          }
-        }
+          for (int u = 0; u < 8; ++u) mx[u] = fmax3(mx[u], s[c + u], s[c + 8 + u]);
         const float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
         const float m_new = (bmax > m_run + 8.f) ? bmax : m_run;  // lazy rescale, 2^8
@@ -320,35 +343,30 @@ __global__ void __launch_bounds__(384, 1)
             tmem_st32(o_addr + 32 * c, o);
           }
         }
-        // pass 2: probabilities, packed in pairs over the S columns already read
-        float sm[8];
+        const f32x2 sl2x2 = f2_make(sl2, sl2);
+        const f32x2 noff = f2_make(-m_use, -m_use);
+        f32x2 sm[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) sm[u] = 0.f;
+        for (int u = 0; u < 4; ++u) sm[u] = 0ull;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          float s[64];
-          tmem_ld64(s_addr + 64 * hf, reinterpret_cast<uint32_t*>(s));
+        for (int c = 0; c < 128; c += 2) {
+          const float2 x = f2_split(f2_fma(f2_make(s[c], s[c + 1]), sl2x2, noff));
+          const float e0 = fast_exp2(x.x), e1 = fast_exp2(x.y);
+          s[c] = e0;
+          s[c + 1] = e1;
+          sm[(c >> 1) & 3] = f2_add(sm[(c >> 1) & 3], f2_make(e0, e1));
+        }
+        // P over the first 64 columns of this tile's S buffer (already read)
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
           uint32_t pk[32];
 #pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            float e0, e1;
-            if (full) {
-              e0 = fast_exp2(fmaf(s[c], sl2, -m_use));
-              e1 = fast_exp2(fmaf(s[c + 1], sl2, -m_use));
-            } else {
-              const int key = kb + 64 * hf + c;
-              e0 = (key >= lo && key < hi) ? fast_exp2(fmaf(s[c], sl2, -m_use)) : 0.f;
-              e1 = (key + 1 >= lo && key + 1 < hi) ? fast_exp2(fmaf(s[c + 1], sl2, -m_use)) : 0.f;
-            }
-            sm[c & 7] += e0;
-            sm[(c + 1) & 7] += e1;
-            pk[c >> 1] = pack2(e0, e1, DT);
-          }
-          tmem_st32(s_addr + 32 * hf, pk);
+          for (int c = 0; c < 32; ++c) pk[c] = pack2(s[64 * h2 + 2 * c], s[64 * h2 + 2 * c + 1], DT);
+          tmem_st32(s_addr + 32 * h2, pk);
         }
         tmem_st_wait();
-        const float rsum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
-        l_run = l_run * alpha + rsum;
+        const float2 r01 = f2_split(f2_add(f2_add(sm[0], sm[1]), f2_add(sm[2], sm[3])));
+        l_run = l_run * alpha + (r01.x + r01.y);
         m_run = m_new;
       }
       tc_fence_before();
@@ -409,25 +427,10 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
     }
-  }
 
-  // ------------------------------------------------------------- teardown
-  if (warp == 0 && lane == 0 && *abort_flag) {
-    for (int st = 0; st < KS && st < issued_k; ++st) {
-      const int j_last = st + ((issued_k - 1 - st) / KS) * KS;
-      mbar_wait(k_full + 8 * st, (j_last / KS) & 1, nullptr, nullptr);
-    }
-    for (int st = 0; st < VS && st < issued_v; ++st) {
-      const int j_last = st + ((issued_v - 1 - st) / VS) * VS;
-      mbar_wait(v_full + 8 * st, (j_last / VS) & 1, nullptr, nullptr);
-    }
-    if (nblk > 0) mbar_wait(q_full, 0, nullptr, nullptr);
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+    // teardown (softmax side): the TMEM release waits for these warps
+    tc_fence_before();
+    __syncthreads();
   }
 }
 

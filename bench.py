@@ -62,6 +62,10 @@ WORKLOADS = {
                                 "H_q=H_kv=16, D=128, bf16, causal"),
     "prefill_gqa": dict(name="prefill", kw={"h_kv": 4}, causal=False, kind="tensor",
                         desc="varlen prefill: 16384 tokens, H_q=16, H_kv=4, D=128, bf16, no mask"),
+    "prefill_d256": dict(name="prefill", kw={"h_kv": 16, "d": 256}, causal=False, kind="tensor",
+                         desc="varlen prefill: 16384 tokens, H_q=H_kv=16, D=256, bf16, no mask"),
+    "decode_d256": dict(name="long_decode", kw={"kv": 65536, "h": 16, "d": 256},
+                        desc="long-context decode MHA: B=1, Q=1, K=65536, H_q=H_kv=16, D=256, bf16"),
     "prefill_gqa_causal": dict(name="prefill", kw={"h_kv": 4}, causal=True, kind="tensor",
                                desc="varlen prefill: 16384 tokens, H_q=16, H_kv=4, D=128, bf16, causal"),
 }

@@ -101,7 +101,7 @@ typedef enum {
  *                 TMA reads never go past these rows (zero fill beyond).
  *  max_seqlen_q   largest Lq_b (sizes the tile grid and the workspace).
  *  h_q, h_kv      query and key/value heads, h_q % h_kv == 0, h_q/h_kv <= 128.
- *  d_qk, d_v      head dims: (64,64) or (128,128) for bf16/fp16;
+ *  d_qk, d_v      head dims: (64,64), (128,128) or (256,256) for bf16/fp16;
  *                 (128,128) or (192,128) for e4m3.
  *  scale          softmax scale; <= 0 selects 1/sqrt(d_qk) (cutlass PR,
  *                 "Implementation": the default scale uses the head dim).
@@ -121,8 +121,9 @@ typedef enum {
  *  flags          FA_KERNEL_* selection, optionally OR FA_RUN_*_ONLY.  AUTO
  *                 picks the CUDA-core kernel for up to 4 rows (queries x
  *                 group) per KV head (2 for e4m3 with d_qk=192), the
- *                 one-tile tcgen05 kernel up to 128 rows and for e4m3, and
- *                 the two-tile tcgen05 kernel beyond 128 rows.
+ *                 one-tile tcgen05 kernel up to 128 rows, for e4m3 and for
+ *                 head dim 256, and the two-tile tcgen05 kernel beyond 128
+ *                 rows (16-bit, head dim <= 128).
  *  stream         cudaStream_t.
  * Returns FA_OK or a negative fa_status.
  */

@@ -136,7 +136,7 @@ int plan_impl(int batch, int max_seqlen_q, int h_q, int h_kv, int num_splits, in
 
 bool dims_supported(int in_dtype, int d_qk, int d_v) {
   if (in_dtype == kE4M3) return (d_qk == 128 || d_qk == 192) && d_v == 128;
-  return (d_qk == 64 && d_v == 64) || (d_qk == 128 && d_v == 128);
+  return (d_qk == 64 && d_v == 64) || (d_qk == 128 && d_v == 128) || (d_qk == 256 && d_v == 256);
 }
 
 }  // namespace
@@ -156,7 +156,7 @@ cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
 
 int simt_max_rows(int dtype, int d_qk, int d_v) {
   if (!dims_supported(dtype, d_qk, d_v)) return 0;
-  if (dtype == kE4M3 && d_qk == 192) return 2;
+  if ((dtype == kE4M3 && d_qk == 192) || d_qk == 256) return 2;
   return 4;
 }
 
@@ -201,6 +201,7 @@ cudaError_t launch_combine(const FwdParams& p, cudaStream_t stream) {
   switch (p.d_v) {
     case 64: return cudaLaunchKernelEx(&cfg, combine_kernel<64>, p);
     case 128: return cudaLaunchKernelEx(&cfg, combine_kernel<128>, p);
+    case 256: return cudaLaunchKernelEx(&cfg, combine_kernel<256>, p);
   }
   return cudaErrorInvalidValue;
 }
@@ -309,7 +310,7 @@ int fa_fwd_splitkv_ex(const void* q, const void* k, const void* v, const int* cu
   if (!dims_supported(in_dtype, d_qk, d_v)) return FA_ERR_UNSUPPORTED;
   if (isnan(scale) || isinf(scale)) return FA_ERR_INVALID_ARG;
   const int kernel_sel = flags & FA_KERNEL_MASK;
-  if (kernel_sel == FA_KERNEL_UMMA2 && in_dtype == kE4M3) return FA_ERR_UNSUPPORTED;
+  if (kernel_sel == FA_KERNEL_UMMA2 && (in_dtype == kE4M3 || d_qk > 128)) return FA_ERR_UNSUPPORTED;
   if (flags & ~(FA_KERNEL_MASK | FA_RUN_PARTIAL_ONLY | FA_RUN_COMBINE_ONLY)) return FA_ERR_INVALID_ARG;
   const bool run_partial = !(flags & FA_RUN_COMBINE_ONLY);
   const bool run_combine = !(flags & FA_RUN_PARTIAL_ONLY);
@@ -385,7 +386,8 @@ int fa_fwd_splitkv_ex(const void* q, const void* k, const void* v, const int* cu
   // More than one 128-row tile per KV head with 16-bit inputs: two tiles per
   // CTA share each K/V block and overlap their softmax with the other tile's
   // MMAs.  Otherwise one tile per CTA.
-  const bool use_umma2 = kernel_sel == FA_KERNEL_UMMA2 || (auto_tc && rows > 128 && in_dtype != kE4M3);
+  const bool use_umma2 =
+      kernel_sel == FA_KERNEL_UMMA2 || (auto_tc && rows > 128 && in_dtype != kE4M3 && d_qk <= 128);
   const bool use_umma = !use_umma2 && (kernel_sel == FA_KERNEL_UMMA || auto_tc);
   if ((unsigned)(batch * h_kv) > 65535u) return FA_ERR_UNSUPPORTED;
   if (run_partial) {

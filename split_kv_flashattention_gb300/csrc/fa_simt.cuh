@@ -59,7 +59,7 @@ struct SimtCfg {
   // already consumed it, so a parity wait can never match a phase two behind
   // (a different warp could still be waiting on that older load).
   static_assert(NS % NW == 0 && NS >= 2 * NW, "stages must be a multiple of the consumer warps");
-  static_assert(NPV <= 2 && NPK <= 4, "head dim too large for this kernel");
+  static_assert(NPV <= 4 && NPK <= 4, "head dim too large for this kernel");
 };
 
 template <int NBYTES>

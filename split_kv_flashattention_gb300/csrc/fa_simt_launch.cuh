@@ -19,10 +19,18 @@ struct SimtStages {
   static constexpr int NS = NS_RAW - NS_RAW % NW;
 };
 
+// Consumer warps: 4, or 2 when one 32-key stage is 32 KB (head dim 256) so
+// that two stages per warp still fit.
+template <int DT, int DQK, int DV>
+struct SimtWarps {
+  static constexpr int STAGE = SimtStages<DT, DQK, DV, 4>::STAGE;
+  static constexpr int NW = STAGE >= 32 * 1024 ? 2 : 4;
+};
+
 template <int DT, int DQK, int DV, int RT>
 cudaError_t launch_simt_one(const FwdParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                             dim3 grid, cudaStream_t stream) {
-  constexpr int NW = 4;
+  constexpr int NW = SimtWarps<DT, DQK, DV>::NW;
   constexpr int NS = SimtStages<DT, DQK, DV, NW>::NS;
   using C = SimtCfg<DT, DQK, DV, RT, NW, NS>;
   auto kern = simt_splitkv_kernel<DT, DQK, DV, RT, NW, NS>;

@@ -102,6 +102,8 @@ def _call_ex(fa, **kw):
     (dict(num_splits=129), -1),                    # more than 128 splits
     (dict(batch=-1), -1),
     (dict(d_qk=96, d_v=96), -2),                   # unsupported head dim
+    (dict(d_qk=256, d_v=128), -2),                 # unequal 16-bit dims
+    (dict(d_qk=256, d_v=256, flags=3), -2),        # two-tile kernel: head dim <= 128
     (dict(d_qk=192, d_v=128), -2),                 # 192 only for e4m3
     (dict(in_dtype=0, out_dtype=1), -2),           # bf16 in, fp16 out
     (dict(in_dtype=7), -1),

@@ -280,3 +280,20 @@ def test_gqa_group_16_prefix(kernel):
     out, lse = run_gpu(inp, num_splits=0, flags=kernel, causal=True)
     o_ref, l_ref = reference(inp, 0.0, True)
     assert_close(inp, out, lse, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dim_256(kernel, dtype, causal):
+    """d=256 (cutlass varlen page, "Tests": d=64, d=256), GQA 2:1, ragged
+    lengths spanning several key blocks and query tiles."""
+    inp = make_inputs([1, 2, 140], [777, 1500, 300], 4, 2, 256, 256, dtype, seed=13)
+    if kernel == fa.FA_KERNEL_UMMA2:
+        with pytest.raises(fa.FaError) as e:
+            run_gpu(inp, causal=causal, num_splits=3, flags=kernel)
+        assert e.value.status == -2
+        return
+    out, lse = run_gpu(inp, causal=causal, num_splits=3, flags=kernel)
+    o_ref, l_ref = reference(inp, 0.0, causal)
+    assert_close(inp, out, lse, o_ref, l_ref)

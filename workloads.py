@@ -136,7 +136,8 @@ def workload(name: str, seed: int = 0, device: str = "cpu", **kw) -> Inputs:
     if name == "long_decode":
         kv = kw.get("kv", 131072)
         h = kw.get("h", 32)
-        return make_inputs([1], [kv], h, h, 128, 128, "bf16", seed, device)
+        d = kw.get("d", 128)
+        return make_inputs([1], [kv], h, h, d, d, "bf16", seed, device)
     if name == "gqa_decode":
         batch = kw.get("batch", 32)
         lens_k = kw.get("lens_k") or gqa_decode_lengths(seed, batch)
@@ -148,7 +149,8 @@ def workload(name: str, seed: int = 0, device: str = "cpu", **kw) -> Inputs:
         return make_inputs([q], [kv], h, h, 192, 128, "e4m3", seed, device)
     if name == "prefill":
         lens = kw.get("lens", PREFILL_LENGTHS)
-        return make_inputs(lens, lens, 16, kw.get("h_kv", 16), 128, 128,
+        d = kw.get("d", 128)
+        return make_inputs(lens, lens, 16, kw.get("h_kv", 16), d, d,
                            kw.get("dtype", "bf16"), seed, device)
     if name == "edge":
         lens = kw.get("lens", EDGE_LENGTHS)

@@ -135,6 +135,30 @@ FA_API int fa_fwd_splitkv_ex(const void* q, const void* k, const void* v, const 
                       const float* descale_q, const float* descale_k, const float* descale_v,
                       int flags, void* stream);
 
+/*
+ * fa_fwd_splitkv_paged -- the same forward pass over a paged K/V cache
+ * (serving-style decode).  The pages this library follows do not describe a
+ * paged layout; this one is the common serving convention:
+ *   k_cache [num_pages, page_size, h_kv, d_qk], v_cache [num_pages, page_size,
+ *   h_kv, d_v] (device, 16-byte aligned), block_table int32 [batch,
+ *   max_pages_per_seq] (device): block_table[b][i] is the page holding keys
+ *   i*page_size .. (i+1)*page_size-1 of sequence b; seqlens_k int32 [batch]
+ *   (device): keys of sequence b.  page_size is a power of two >= 32.
+ * Queries, outputs, masks, splits, dtypes, workspace and flags are as in
+ * fa_fwd_splitkv_ex (fa_fwd_splitkv_workspace_size applies unchanged).  A
+ * page index outside [0, num_pages) or a sequence longer than
+ * max_pages_per_seq*page_size is skipped and reported as FA_ERR_DEVICE_ARG.
+ */
+FA_API int fa_fwd_splitkv_paged(const void* q, const void* k_cache, const void* v_cache,
+                                const int* cu_seqlens_q, const int* seqlens_k,
+                                const int* block_table, int batch, int total_q, int num_pages,
+                                int page_size, int max_pages_per_seq, int max_seqlen_q, int h_q,
+                                int h_kv, int d_qk, int d_v, float scale, int causal,
+                                int window_left, int num_splits, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes, int in_dtype,
+                                int out_dtype, const float* descale_q, const float* descale_k,
+                                const float* descale_v, int flags, void* stream);
+
 /* bf16 in / bf16 out shorthand of fa_fwd_splitkv_ex with automatic kernel
  * selection; the workspace is trusted to be large enough. */
 FA_API int fa_fwd_splitkv(const void* q, const void* k, const void* v, const int* cu_seqlens_q,

@@ -28,6 +28,8 @@ Modules:
   the LSE-weighted combine of partials (the split-KV identity).
 * ``planner``    -- the integer split planner and per-split key ranges, the
   host/device rule that the library must reproduce bit for bit.
+* ``paged``      -- the paged K/V layout as plain indexing (gather pages back
+  into packed K/V), for the paged-cache entry point.
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
 against closed forms, hand-worked fixtures in ``tests/golden/``, brute force
@@ -46,6 +48,7 @@ from .attention import (  # noqa: F401
     partial_attention,
     split_attention,
 )
+from .paged import gather_paged_kv  # noqa: F401
 from .planner import (  # noqa: F401
     BLOCK_N,
     M_TILE,

@@ -23,6 +23,7 @@ __all__ = [
     "fa_get_device_error", "fa_status_string", "fa_version", "forward",
     "FA_KERNEL_AUTO", "FA_KERNEL_SIMT", "FA_KERNEL_UMMA", "FA_KERNEL_UMMA2", "FA_RUN_PARTIAL_ONLY",
     "FA_RUN_COMBINE_ONLY", "DTYPE_CODES", "fa_fwd_splitkv_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "fa_fwd_splitkv_paged", "FA_KERNEL_UMMA2",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libfa_splitkv.so")
@@ -33,7 +34,7 @@ DTYPE_CODES = {torch.bfloat16: 0, torch.float16: 1, torch.float8_e4m3fn: 2}
 EXPORTED = (
     "fa_fwd_splitkv_ex", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_plan",
     "fa_debug_split_ranges", "fa_get_device_error", "fa_status_string", "fa_version",
-    "fa_fwd_splitkv_noalloc",
+    "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_paged",
 )
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -75,6 +76,11 @@ def library() -> ctypes.CDLL:
     lib.fa_fwd_splitkv_noalloc.argtypes = [
         _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
         _c_float, _c_int, _c_int, _c_int, _vp, _vp, _c_int, _c_int, _vp, _vp, _vp, _c_int, _vp]
+    lib.fa_fwd_splitkv_paged.restype = _c_int
+    lib.fa_fwd_splitkv_paged.argtypes = [
+        _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+        _c_int, _c_int, _c_int, _c_float, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_size, _c_int,
+        _c_int, _vp, _vp, _vp, _c_int, _vp]
     lib.fa_fwd_splitkv_workspace_size.restype = _c_size
     lib.fa_fwd_splitkv_workspace_size.argtypes = [_c_int] * 6
     lib.fa_plan.restype = _c_int
@@ -187,6 +193,28 @@ def fa_fwd_splitkv_noalloc(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: in
         DTYPE_CODES[q.dtype], DTYPE_CODES[out.dtype], _ptr(descale_q), _ptr(descale_k),
         _ptr(descale_v), int(flags), _stream(stream))
     _check(st, "fa_fwd_splitkv_noalloc")
+
+
+def fa_fwd_splitkv_paged(q, k_cache, v_cache, cu_seqlens_q, seqlens_k, block_table,
+                         max_seqlen_q: int, out, lse=None, workspace=None, scale: float = 0.0,
+                         causal: bool = False, window_left: int = -1, num_splits: int = 0,
+                         descale_q=None, descale_k=None, descale_v=None,
+                         flags: int = FA_KERNEL_AUTO, stream=None):
+    """Calls fa_fwd_splitkv_paged: K/V caches [num_pages, page_size, h_kv, d],
+    block_table int32 [batch, max_pages], seqlens_k int32 [batch]."""
+    total_q, h_q, d_qk = q.shape
+    num_pages, page_size, h_kv, _ = k_cache.shape
+    d_v = v_cache.shape[3]
+    batch = cu_seqlens_q.numel() - 1
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = library().fa_fwd_splitkv_paged(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q), _ptr(seqlens_k),
+        _ptr(block_table), batch, total_q, num_pages, page_size, block_table.shape[1],
+        max_seqlen_q, h_q, h_kv, d_qk, d_v, float(scale), int(causal), int(window_left),
+        int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, DTYPE_CODES[q.dtype],
+        DTYPE_CODES[out.dtype], _ptr(descale_q), _ptr(descale_k), _ptr(descale_v), int(flags),
+        _stream(stream))
+    _check(st, "fa_fwd_splitkv_paged")
 
 
 def fa_fwd_splitkv(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, out, lse=None,

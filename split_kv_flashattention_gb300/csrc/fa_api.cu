@@ -293,13 +293,21 @@ int fa_debug_split_ranges(const int* cu_seqlens_q, const int* cu_seqlens_k, int 
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-int fa_fwd_splitkv_ex(const void* q, const void* k, const void* v, const int* cu_seqlens_q,
-                      const int* cu_seqlens_k, int batch, int total_q, int total_k,
-                      int max_seqlen_q, int h_q, int h_kv, int d_qk, int d_v, float scale,
-                      int causal, int window_left, int num_splits, void* out, float* lse,
-                      void* workspace, size_t workspace_bytes, int in_dtype, int out_dtype,
-                      const float* descale_q, const float* descale_k, const float* descale_v,
-                      int flags, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of fa_fwd_splitkv_ex (contiguous K/V addressed by cu_seqlens_k)
+// and fa_fwd_splitkv_paged (page pools addressed by block_table/seqlens_k,
+// page_size > 0).
+int fwd_impl(const void* q, const void* k, const void* v, const int* cu_seqlens_q,
+             const int* cu_seqlens_k, int batch, int total_q, int total_k, int max_seqlen_q,
+             int h_q, int h_kv, int d_qk, int d_v, float scale, int causal, int window_left,
+             int num_splits, void* out, float* lse, void* workspace, size_t workspace_bytes,
+             int in_dtype, int out_dtype, const float* descale_q, const float* descale_k,
+             const float* descale_v, int flags, void* stream, const int* block_table,
+             const int* seqlens_k, int max_pages, int page_size) {
+  const bool paged = page_size > 0;
   // ---- argument validation (synchronous, before any launch)
   if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0) return FA_ERR_INVALID_ARG;
   if (h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || h_q / h_kv > 128) return FA_ERR_INVALID_ARG;
@@ -316,7 +324,9 @@ int fa_fwd_splitkv_ex(const void* q, const void* k, const void* v, const int* cu
   const bool run_combine = !(flags & FA_RUN_PARTIAL_ONLY);
   if (!run_partial && !run_combine) return FA_ERR_INVALID_ARG;
   if (batch == 0 || max_seqlen_q == 0 || total_q == 0) return FA_OK;  // nothing to compute
-  if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out) return FA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !cu_seqlens_q || !out) return FA_ERR_INVALID_ARG;
+  if (!paged && !cu_seqlens_k) return FA_ERR_INVALID_ARG;
+  if (paged && (!block_table || !seqlens_k || max_pages <= 0)) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return FA_ERR_INVALID_ARG;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_INVALID_ARG;
   const int es = in_dtype == kE4M3 ? 1 : 2;
@@ -375,6 +385,10 @@ int fa_fwd_splitkv_ex(const void* q, const void* k, const void* v, const int* cu
   p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)d_qk);
   p.out_dtype = out_dtype;
   p.slots = (int)slots;
+  p.block_table = paged ? block_table : nullptr;
+  p.seqlens_k = paged ? seqlens_k : nullptr;
+  p.max_pages = paged ? max_pages : 0;
+  p.page_size = paged ? page_size : 0;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -392,7 +406,8 @@ int fa_fwd_splitkv_ex(const void* q, const void* k, const void* v, const int* cu
   if ((unsigned)(batch * h_kv) > 65535u) return FA_ERR_UNSUPPORTED;
   if (run_partial) {
     CUtensorMap tmK, tmV;
-    const int box_keys = (use_umma || use_umma2) ? kBlockN : 32;
+    int box_keys = (use_umma || use_umma2) ? kBlockN : 32;
+    if (paged && page_size < box_keys) box_keys = page_size;  // one load per page piece
     st = make_tmap_3d(&tmK, k, in_dtype, d_qk, h_kv, total_k, box_keys);
     if (st != FA_OK) return st;
     st = make_tmap_3d(&tmV, v, in_dtype, d_v, h_kv, total_k, box_keys);
@@ -430,6 +445,45 @@ int fa_fwd_splitkv_ex(const void* q, const void* k, const void* v, const int* cu
     if (e != cudaSuccess) return FA_ERR_CUDA;
   }
   return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd_splitkv_ex(const void* q, const void* k, const void* v, const int* cu_seqlens_q,
+                      const int* cu_seqlens_k, int batch, int total_q, int total_k,
+                      int max_seqlen_q, int h_q, int h_kv, int d_qk, int d_v, float scale,
+                      int causal, int window_left, int num_splits, void* out, float* lse,
+                      void* workspace, size_t workspace_bytes, int in_dtype, int out_dtype,
+                      const float* descale_q, const float* descale_k, const float* descale_v,
+                      int flags, void* stream) {
+  return fwd_impl(q, k, v, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, max_seqlen_q,
+                  h_q, h_kv, d_qk, d_v, scale, causal, window_left, num_splits, out, lse,
+                  workspace, workspace_bytes, in_dtype, out_dtype, descale_q, descale_k,
+                  descale_v, flags, stream, nullptr, nullptr, 0, 0);
+}
+
+int fa_fwd_splitkv_paged(const void* q, const void* k_cache, const void* v_cache,
+                         const int* cu_seqlens_q, const int* seqlens_k, const int* block_table,
+                         int batch, int total_q, int num_pages, int page_size,
+                         int max_pages_per_seq, int max_seqlen_q, int h_q, int h_kv, int d_qk,
+                         int d_v, float scale, int causal, int window_left, int num_splits,
+                         void* out, float* lse, void* workspace, size_t workspace_bytes,
+                         int in_dtype, int out_dtype, const float* descale_q,
+                         const float* descale_k, const float* descale_v, int flags,
+                         void* stream) {
+  if (page_size < 32 || (page_size & (page_size - 1)) != 0 || page_size > (1 << 20))
+    return FA_ERR_INVALID_ARG;
+  if (num_pages < 0 || max_pages_per_seq < 0 || (long long)num_pages * page_size > 0x7fffffffLL)
+    return FA_ERR_INVALID_ARG;
+  if (batch > 0 && max_seqlen_q > 0 && total_q > 0 && (num_pages == 0 || max_pages_per_seq == 0))
+    return FA_ERR_INVALID_ARG;
+  return fwd_impl(q, k_cache, v_cache, cu_seqlens_q, nullptr, batch, total_q,
+                  num_pages * page_size, max_seqlen_q, h_q, h_kv, d_qk, d_v, scale, causal,
+                  window_left, num_splits, out, lse, workspace, workspace_bytes, in_dtype,
+                  out_dtype, descale_q, descale_k, descale_v, flags, stream, block_table,
+                  seqlens_k, max_pages_per_seq, page_size);
 }
 
 int fa_fwd_splitkv(const void* q, const void* k, const void* v, const int* cu_seqlens_q,

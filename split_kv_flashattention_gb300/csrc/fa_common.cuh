@@ -41,6 +41,14 @@ struct FwdParams {
   int out_dtype;    // DType of O
   int slots;        // batch * max_seqlen_q
   int tile_rows;    // rows (query, head pairs) per CTA tile
+  // Paged K/V (page_size > 0): K/V are page pools [num_pages*page_size, h_kv, d];
+  // key j of sequence b lives in pool row
+  //   block_table[b*max_pages + j/page_size]*page_size + j%page_size
+  // and seqlens_k[b] gives the sequence's key count (cu_k is unused).
+  const int* block_table;
+  const int* seqlens_k;
+  int max_pages;
+  int page_size;    // 0: contiguous packed K/V addressed through cu_k
 };
 
 struct SeqInfo {
@@ -53,11 +61,43 @@ struct SeqInfo {
 __device__ __forceinline__ bool load_seq(const FwdParams& p, int b, SeqInfo& s) {
   s.q0 = __ldg(p.cu_q + b);
   s.lq = __ldg(p.cu_q + b + 1) - s.q0;
+  if (p.page_size > 0) {
+    s.k0 = 0;
+    s.lk = __ldg(p.seqlens_k + b);
+    return s.q0 >= 0 && s.lq >= 0 && s.lk >= 0 && s.lq <= p.max_seqlen_q &&
+           s.q0 + s.lq <= p.total_q && (long long)s.lk <= (long long)p.max_pages * p.page_size;
+  }
   s.k0 = __ldg(p.cu_k + b);
   s.lk = __ldg(p.cu_k + b + 1) - s.k0;
   bool ok = s.q0 >= 0 && s.lq >= 0 && s.k0 >= 0 && s.lk >= 0 && s.lq <= p.max_seqlen_q &&
             s.q0 + s.lq <= p.total_q && s.k0 + s.lk <= p.total_k;
   return ok;
+}
+
+// First K/V row of a load of `box` rows starting at key `key` (sequence-
+// local) of sequence b.  For paged K/V the caller keeps the load inside one
+// page (key % box == 0, box <= page_size, both powers of two).  Loads that
+// start past the sequence's keys (tails of the last block; every such row is
+// masked) read the sequence's last box instead, so they never index the
+// block table past the sequence's pages and always bring finite values.  A
+// page index outside the pool reads row 0 and is reported through the error
+// word.
+__device__ __forceinline__ int kv_row(const FwdParams& p, const SeqInfo& s, int b, int key,
+                                      int box) {
+  if (p.page_size <= 0) return s.k0 + key;
+  if (key >= s.lk) key = (s.lk - 1) - ((s.lk - 1) % box);
+  const int pg = __ldg(p.block_table + (size_t)b * p.max_pages + key / p.page_size);
+  if (pg < 0 || (long long)(pg + 1) * p.page_size > p.total_k) {
+    if (p.err) atomicCAS(p.err, 0, -6);
+    return 0;
+  }
+  return pg * p.page_size + (key & (p.page_size - 1));
+}
+
+// First key of a tile's load schedule: the split's first key, rounded down to
+// the load granularity in paged mode so no load crosses a page.
+__device__ __forceinline__ int load_base(const FwdParams& p, int k0, int granularity) {
+  return p.page_size > 0 ? k0 - (k0 % granularity) : k0;
 }
 
 // Allowed keys [lo, hi) of query i in a (lq, lk) sequence: everything without

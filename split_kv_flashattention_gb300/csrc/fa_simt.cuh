@@ -110,7 +110,8 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   int k0, k1;
   tile_split_range(i_lo, i_hi, sq.lq, sq.lk, p.causal, p.window_left, p.num_splits, split, k0,
                    k1);
-  const int nchunks = k1 > k0 ? (k1 - k0 + C::KC - 1) / C::KC : 0;
+  const int key0 = load_base(p, k0, C::KC);  // first key of chunk 0
+  const int nchunks = k1 > k0 ? (k1 - key0 + C::KC - 1) / C::KC : 0;
 
   const uint32_t bar_full = sbase + C::OFF_BAR;
   const uint32_t bar_empty = bar_full + NS * 8;
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         const uint32_t dst = sbase + st * C::STAGE;
         const uint32_t fb = bar_full + 8 * st;
         mbar_arrive_expect_tx(fb, C::STAGE);
-        const int row = sq.k0 + k0 + c * C::KC;
+        const int row = kv_row(p, sq, b, key0 + c * C::KC, C::KC);
 #pragma unroll
         for (int pk = 0; pk < C::NPK; ++pk)
           tma_load_3d(dst + pk * C::PANEL, &tmK, fb, pk * C::PANEL_ELEMS, kh, row, pol);
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       if (!__all_sync(0xffffffffu, ok)) break;  // leave together: shuffles below need all lanes
       const uint8_t* kbase = smem + st * C::STAGE;
       const uint8_t* vbase = kbase + C::NPK * C::PANEL;
-      const int key_base = k0 + c * C::KC;
+      const int key_base = key0 + c * C::KC;
 
       float sc[RT][4];
 #pragma unroll

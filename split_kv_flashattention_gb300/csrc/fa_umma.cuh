@@ -169,7 +169,11 @@ __global__ void __launch_bounds__(192, 1)
   int k0, k1;
   tile_split_range(q_start, q_start + nq - 1, sq.lq, sq.lk, p.causal, p.window_left, p.num_splits,
                    split, k0, k1);
-  const int nblk = k1 > k0 ? (k1 - k0 + kBlockN - 1) / kBlockN : 0;
+  const int kb0 = load_base(p, k0, kBlockN);  // first key of block 0
+  const int nblk = k1 > k0 ? (k1 - kb0 + kBlockN - 1) / kBlockN : 0;
+  // TMA boxes per 128-key block: several when K/V pages are smaller than 128
+  const int box_rows = (p.page_size > 0 && p.page_size < kBlockN) ? p.page_size : kBlockN;
+  const int nsub = kBlockN / box_rows;
 
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t q_full = bar0;
@@ -235,8 +239,10 @@ __global__ void __launch_bounds__(192, 1)
           mbar_arrive_expect_tx(k_full + 8 * st, C::K_STAGE);
 #pragma unroll
           for (int pk = 0; pk < C::NPQ; ++pk)
-            tma_load_3d(dst + pk * C::PANEL, &tmK, k_full + 8 * st, pk * C::PANEL_ELEMS, kh,
-                        sq.k0 + k0 + j * kBlockN, pol_kv);
+            for (int sb = 0; sb < nsub; ++sb)
+              tma_load_3d(dst + pk * C::PANEL + sb * box_rows * 128, &tmK, k_full + 8 * st,
+                          pk * C::PANEL_ELEMS, kh, kv_row(p, sq, b, kb0 + j * kBlockN + sb * box_rows, box_rows),
+                          pol_kv);
           issued_k = j + 1;
         }
         if (j >= 1) {
@@ -247,8 +253,10 @@ __global__ void __launch_bounds__(192, 1)
           mbar_arrive_expect_tx(v_full + 8 * st, C::V_STAGE);
 #pragma unroll
           for (int pv = 0; pv < C::NPV; ++pv)
-            tma_load_3d(dst + pv * C::PANEL, &tmV, v_full + 8 * st, pv * C::PANEL_ELEMS, kh,
-                        sq.k0 + k0 + jv * kBlockN, pol_kv);
+            for (int sb = 0; sb < nsub; ++sb)
+              tma_load_3d(dst + pv * C::PANEL + sb * box_rows * 128, &tmV, v_full + 8 * st,
+                          pv * C::PANEL_ELEMS, kh, kv_row(p, sq, b, kb0 + jv * kBlockN + sb * box_rows, box_rows),
+                          pol_kv);
           issued_v = jv + 1;
         }
       }
@@ -346,7 +354,7 @@ __global__ void __launch_bounds__(192, 1)
         if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
         const uint32_t s_addr = tmem + lane_base + ((j & 1) ? C::TM_S1 : C::TM_S0);
-        const int kb = k0 + j * kBlockN;
+        const int kb = kb0 + j * kBlockN;
         tmem_ld128(s_addr, reinterpret_cast<uint32_t*>(s));
         // Max of the raw scores (the scale is positive): eight independent
         // chains; keys outside [lo, hi) only exist in boundary blocks.

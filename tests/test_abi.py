@@ -129,3 +129,36 @@ def test_empty_problem_is_a_noop(fa):
     assert _call_ex(fa, batch=0) == 0
     assert _call_ex(fa, max_seqlen_q=0) == 0
     assert _call_ex(fa, total_q=0) == 0
+
+
+def _call_paged(fa, **kw):
+    a = dict(q=0x1000, kc=0x2000, vc=0x3000, cu_q=0x4000, seqlens=0x5000, table=0x5800, batch=2,
+             total_q=2, num_pages=8, page_size=64, max_pages=4, max_seqlen_q=1, h_q=8, h_kv=2,
+             d_qk=128, d_v=128, scale=0.0, causal=0, window_left=-1, num_splits=1, out=0x6000,
+             lse=0x7000, ws=0, ws_bytes=0, in_dtype=0, out_dtype=0, flags=0)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return fa.library().fa_fwd_splitkv_paged(
+        vp(a["q"]), vp(a["kc"]), vp(a["vc"]), vp(a["cu_q"]), vp(a["seqlens"]), vp(a["table"]),
+        a["batch"], a["total_q"], a["num_pages"], a["page_size"], a["max_pages"],
+        a["max_seqlen_q"], a["h_q"], a["h_kv"], a["d_qk"], a["d_v"], a["scale"], a["causal"],
+        a["window_left"], a["num_splits"], vp(a["out"]), vp(a["lse"]), vp(a["ws"]), a["ws_bytes"],
+        a["in_dtype"], a["out_dtype"], vp(0), vp(0), vp(0), a["flags"], vp(0))
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(page_size=48), -1),        # not a power of two
+    (dict(page_size=16), -1),        # below the 32-row load granularity
+    (dict(table=0), -1),             # no block table
+    (dict(seqlens=0), -1),           # no key counts
+    (dict(num_pages=0), -1),         # empty pool
+    (dict(max_pages=0), -1),
+    (dict(d_qk=96, d_v=96), -2),
+    (dict(kc=0x2008), -1),           # unaligned cache
+])
+def test_paged_argument_errors(fa, kw, status):
+    assert _call_paged(fa, **kw) == status
+
+
+def test_paged_empty_problem_is_a_noop(fa):
+    assert _call_paged(fa, batch=0) == 0

@@ -467,3 +467,48 @@ def test_planted_mistakes_are_caught(mutant):
             caught = True
             break
     assert caught, mutant.__name__
+
+
+# ------------------------------------------------------------- paged K/V
+
+def test_gather_paged_kv_inverts_a_scatter():
+    """Scatter packed K/V into pages in a shuffled order (written here as a
+    separate procedure), then the oracle's gather must give the packed K/V
+    back exactly, with the sequences' cu_seqlens."""
+    rng = np.random.default_rng(30)
+    lens = [5, 0, 17, 8]
+    page_size, h, d = 4, 2, 3
+    total = sum(lens)
+    k = torch.from_numpy(rng.standard_normal((total, h, d)))
+    v = torch.from_numpy(rng.standard_normal((total, h, d + 1)))
+    need = [-(-n // page_size) for n in lens]
+    num_pages = sum(need) + 2
+    perm = rng.permutation(num_pages)
+    kc = torch.full((num_pages, page_size, h, d), float("nan"), dtype=torch.float64)
+    vc = torch.full((num_pages, page_size, h, d + 1), float("nan"), dtype=torch.float64)
+    table = np.zeros((len(lens), max(need)), dtype=np.int32)
+    used, start = 0, 0
+    for b, n in enumerate(lens):
+        for pi in range(need[b]):
+            page = int(perm[used])
+            used += 1
+            table[b, pi] = page
+            rows = range(pi * page_size, min(n, (pi + 1) * page_size))
+            for r, j in enumerate(rows):
+                kc[page, r] = k[start + j]
+                vc[page, r] = v[start + j]
+        start += n
+    kg, vg, cu = oracle.gather_paged_kv(kc, vc, table, lens)
+    assert torch.equal(kg, k) and torch.equal(vg, v)
+    assert cu.tolist() == [0, 5, 5, 22, 30]
+
+
+def test_gather_paged_kv_hand_case():
+    """Page size 2, two sequences: seq 0 keys 0..2 in pages (3, 0); seq 1 key
+    0 in page 1."""
+    kc = torch.arange(4 * 2 * 1 * 1, dtype=torch.float64).view(4, 2, 1, 1)
+    vc = -kc
+    k, v, cu = oracle.gather_paged_kv(kc, vc, [[3, 0], [1, 0]], [3, 1])
+    assert k.flatten().tolist() == [6.0, 7.0, 0.0, 2.0]
+    assert v.flatten().tolist() == [-6.0, -7.0, -0.0, -2.0]
+    assert cu.tolist() == [0, 3, 4]

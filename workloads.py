@@ -156,3 +156,57 @@ def workload(name: str, seed: int = 0, device: str = "cpu", **kw) -> Inputs:
         lens = kw.get("lens", EDGE_LENGTHS)
         return make_inputs(lens, lens, 8, 2, 128, 128, kw.get("dtype", "bf16"), seed, device)
     raise KeyError(name)
+
+
+@dataclasses.dataclass
+class PagedInputs:
+    q: torch.Tensor
+    k_cache: torch.Tensor       # [num_pages, page_size, h_kv, d_qk]
+    v_cache: torch.Tensor       # [num_pages, page_size, h_kv, d_v]
+    block_table: torch.Tensor   # int32 [batch, max_pages]
+    seqlens_k: torch.Tensor     # int32 [batch]
+    cu_seqlens_q: torch.Tensor
+    max_seqlen_q: int
+    h_q: int
+    h_kv: int
+    dtype: str
+    page_size: int
+    descale_q: float = 1.0
+    descale_k: float = 1.0
+    descale_v: float = 1.0
+
+    @property
+    def batch(self) -> int:
+        return int(self.cu_seqlens_q.numel()) - 1
+
+    @property
+    def d_v(self) -> int:
+        return int(self.v_cache.shape[3])
+
+
+def make_paged_inputs(lens_q, lens_k, h_q: int, h_kv: int, d_qk: int, d_v: int,
+                      page_size: int, dtype: str = "bf16", seed: int = 0,
+                      spare_pages: int = 3) -> PagedInputs:
+    """Q packed as usual; K/V in a pool of pages (the sequences' pages plus
+    `spare_pages` unused ones) handed out in a seeded random order; unused
+    block-table slots hold page 0."""
+    need = [-(-int(n) // page_size) for n in lens_k]
+    num_pages = sum(need) + spare_pages
+    max_pages = max(need + [1])
+    gen = torch.Generator().manual_seed(seed)
+    t = DTYPES[dtype]
+    q = _randn_chunked(gen, (int(sum(lens_q)), h_q, d_qk), t)
+    k_cache = _randn_chunked(gen, (num_pages, page_size, h_kv, d_qk), t)
+    v_cache = _randn_chunked(gen, (num_pages, page_size, h_kv, d_v), t)
+    order = np.random.default_rng(seed).permutation(num_pages).tolist()
+    table = np.zeros((len(lens_k), max_pages), dtype=np.int32)
+    pos = 0
+    for b, n in enumerate(need):
+        table[b, :n] = order[pos:pos + n]
+        pos += n
+    return PagedInputs(q=q, k_cache=k_cache, v_cache=v_cache,
+                       block_table=torch.from_numpy(table),
+                       seqlens_k=torch.tensor([int(n) for n in lens_k], dtype=torch.int32),
+                       cu_seqlens_q=cu_seqlens(lens_q),
+                       max_seqlen_q=max([int(x) for x in lens_q] + [0]), h_q=h_q, h_kv=h_kv,
+                       dtype=dtype, page_size=page_size)

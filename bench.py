@@ -66,6 +66,9 @@ WORKLOADS = {
                          desc="varlen prefill: 16384 tokens, H_q=H_kv=16, D=256, bf16, no mask"),
     "decode_d256": dict(name="long_decode", kw={"kv": 65536, "h": 16, "d": 256},
                         desc="long-context decode MHA: B=1, Q=1, K=65536, H_q=H_kv=16, D=256, bf16"),
+    "paged_decode": dict(name="gqa_decode", kw={}, paged=64,
+                         desc="batched GQA decode varlen over a paged K/V cache: B=32, Q=1, H_q=32, "
+                              "H_kv=8, D=128, K lengths U[1024,32768] seed 0, 64-key pages, bf16"),
     "prefill_gqa_causal": dict(name="prefill", kw={"h_kv": 4}, causal=True, kind="tensor",
                                desc="varlen prefill: 16384 tokens, H_q=16, H_kv=4, D=128, bf16, causal"),
 }
@@ -156,6 +159,30 @@ def job_throughput(units_per_rank: float, world: int, ms_per_step: float) -> flo
     (weak scaling), so the units of all ranks are divided by the slowest
     rank's step time.  Returned per second, in units / 1e12."""
     return world * units_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
+def to_paged(inp, page_size, dev):
+    """Scatter the packed K/V of `inp` into a pool of pages handed out in a
+    seeded random order; returns (k_cache, v_cache, block_table, seqlens_k)."""
+    import numpy as np
+    cu = inp.cu_seqlens_k.tolist()
+    lens = [cu[b + 1] - cu[b] for b in range(len(cu) - 1)]
+    need = [-(-n // page_size) for n in lens]
+    num_pages = sum(need)
+    order = torch.from_numpy(np.random.default_rng(0).permutation(num_pages)).to(dev)
+    kc = torch.zeros((num_pages, page_size) + tuple(inp.k.shape[1:]), dtype=inp.k.dtype, device=dev)
+    vc = torch.zeros((num_pages, page_size) + tuple(inp.v.shape[1:]), dtype=inp.v.dtype, device=dev)
+    table = torch.zeros((len(lens), max(need)), dtype=torch.int32)
+    pos = 0
+    for b, n in enumerate(lens):
+        pages = order[pos:pos + need[b]]
+        table[b, :need[b]] = pages.cpu().to(torch.int32)
+        for i in range(need[b]):
+            rows = min(page_size, n - i * page_size)
+            kc[pages[i], :rows] = inp.k[cu[b] + i * page_size: cu[b] + i * page_size + rows]
+            vc[pages[i], :rows] = inp.v[cu[b] + i * page_size: cu[b] + i * page_size + rows]
+        pos += need[b]
+    return kc, vc, table.to(dev), torch.tensor(lens, dtype=torch.int32, device=dev)
 
 
 def parse():
@@ -395,6 +422,10 @@ def main():
     inp = workload(spec["name"], device=str(dev), **kw)
     q, k, v = inp.q, inp.k, inp.v
     cq, ck = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev)
+    paged = spec.get("paged", 0)
+    if paged:
+        # the same keys, scattered into a shuffled page pool
+        kc, vc, bt, sk = to_paged(inp, paged, dev)
     out_dtype = torch.bfloat16 if inp.dtype == "e4m3" else q.dtype
     out = torch.empty((q.shape[0], inp.h_q, inp.d_v), dtype=out_dtype, device=dev)
     lse = torch.empty((inp.h_q, q.shape[0]), dtype=torch.float32, device=dev)
@@ -413,7 +444,7 @@ def main():
     if args.kernel == "auto":
         if rows <= simt_rows:
             kern_tag = "simt_splitkv"
-        elif rows > 128 and inp.dtype != "e4m3":
+        elif rows > 128 and inp.dtype != "e4m3" and inp.d_qk <= 128:
             kern_tag = "umma2_splitkv"
         else:
             kern_tag = "umma_splitkv"
@@ -421,6 +452,10 @@ def main():
         kern_tag = {"simt": "simt_splitkv", "umma": "umma_splitkv", "umma2": "umma2_splitkv"}[args.kernel]
 
     def call(flags):
+        if paged:
+            fa.fa_fwd_splitkv_paged(q, kc, vc, cq, sk, bt, inp.max_seqlen_q, out, lse, ws, 0.0,
+                                    causal, -1, args.num_splits, dq, dk, dv, flags, stream)
+            return
         fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, inp.max_seqlen_q, out, lse, ws, 0.0, causal, -1,
                              args.num_splits, dq, dk, dv, flags, stream)
 
@@ -505,19 +540,17 @@ def main():
 
     # ---- end to end through the public call with host buffers
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
-    hq, hk, hv = (x.cpu().pin_memory() for x in (inp.q, inp.k, inp.v))
-    hcq, hck = inp.cu_seqlens_q.pin_memory(), inp.cu_seqlens_k.pin_memory()
+    # the step's inputs: Q and cu_seqlens_q, and K/V with their index arrays
+    dev_in = [q, cq] + ([kc, vc, bt, sk] if paged else [k, v, ck])
+    host_in = [x.cpu().pin_memory() for x in dev_in]
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hcq, hck))
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
     d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
 
     def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        cq.copy_(hcq, non_blocking=True)
-        ck.copy_(hck, non_blocking=True)
+        for d_t, h_t in zip(dev_in, host_in):
+            d_t.copy_(h_t, non_blocking=True)
         call(kernel_flag)
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)

@@ -160,13 +160,19 @@ int simt_max_rows(int dtype, int d_qk, int d_v) {
   return 4;
 }
 
-cudaError_t launch_simt(int dtype, int d_qk, int d_v, int rt, const FwdParams& p,
+cudaError_t launch_simt(int dtype, int d_qk, int d_v, int rt, bool ordered, const FwdParams& p,
                         const CUtensorMap& tmK, const CUtensorMap& tmV, dim3 grid,
                         cudaStream_t stream) {
   switch (dtype) {
-    case kBF16: return launch_simt_bf16(d_qk, d_v, rt, p, tmK, tmV, grid, stream);
-    case kFP16: return launch_simt_fp16(d_qk, d_v, rt, p, tmK, tmV, grid, stream);
-    case kE4M3: return launch_simt_e4m3(d_qk, d_v, rt, p, tmK, tmV, grid, stream);
+    case kBF16:
+      return ordered ? launch_simt_t<kBF16, true>(d_qk, d_v, rt, p, tmK, tmV, grid, stream)
+                     : launch_simt_t<kBF16, false>(d_qk, d_v, rt, p, tmK, tmV, grid, stream);
+    case kFP16:
+      return ordered ? launch_simt_t<kFP16, true>(d_qk, d_v, rt, p, tmK, tmV, grid, stream)
+                     : launch_simt_t<kFP16, false>(d_qk, d_v, rt, p, tmK, tmV, grid, stream);
+    case kE4M3:
+      return ordered ? launch_simt_t<kE4M3, true>(d_qk, d_v, rt, p, tmK, tmV, grid, stream)
+                     : launch_simt_t<kE4M3, false>(d_qk, d_v, rt, p, tmK, tmV, grid, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -389,6 +395,8 @@ int fwd_impl(const void* q, const void* k, const void* v, const int* cu_seqlens_
   p.seqlens_k = paged ? seqlens_k : nullptr;
   p.max_pages = paged ? max_pages : 0;
   p.page_size = paged ? page_size : 0;
+  p.page_shift = 0;
+  while (paged && (1 << p.page_shift) < page_size) ++p.page_shift;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -435,7 +443,10 @@ int fwd_impl(const void* q, const void* k, const void* v, const int* cu_seqlens_
       while (rt < rows && rt < rt_max) rt *= 2;
       p.tile_rows = rt;
       dim3 grid((unsigned)ceil_div(rows, rt), (unsigned)(batch * h_kv), (unsigned)ns);
-      e = launch_simt(in_dtype, d_qk, d_v, rt, p, tmK, tmV, grid, s);
+      // Longest sequence first pays off once there are several sequences of
+      // different lengths to balance; one sequence keeps the grid order.
+      const bool ordered = batch > 1 && batch <= kMaxRankedSeqs;
+      e = launch_simt(in_dtype, d_qk, d_v, rt, ordered, p, tmK, tmV, grid, s);
     }
     if (e != cudaSuccess) return FA_ERR_CUDA;
   }
@@ -473,7 +484,7 @@ int fa_fwd_splitkv_paged(const void* q, const void* k_cache, const void* v_cache
                          int in_dtype, int out_dtype, const float* descale_q,
                          const float* descale_k, const float* descale_v, int flags,
                          void* stream) {
-  if (page_size < 32 || (page_size & (page_size - 1)) != 0 || page_size > (1 << 20))
+  if (page_size < kMinPage || (page_size & (page_size - 1)) != 0 || page_size > (1 << 20))
     return FA_ERR_INVALID_ARG;
   if (num_pages < 0 || max_pages_per_seq < 0 || (long long)num_pages * page_size > 0x7fffffffLL)
     return FA_ERR_INVALID_ARG;

@@ -15,6 +15,8 @@ namespace fa {
 
 constexpr int kBlockN = 128;    // keys per split block
 constexpr int kMaxSplits = 128;
+constexpr int kMinPage = 32;                 // smallest page of a paged K/V cache
+constexpr int kMaxSub = kBlockN / kMinPage;  // page-sized loads per key block, at most
 
 enum DType : int { kBF16 = 0, kFP16 = 1, kE4M3 = 2 };
 
@@ -49,6 +51,7 @@ struct FwdParams {
   const int* seqlens_k;
   int max_pages;
   int page_size;    // 0: contiguous packed K/V addressed through cu_k
+  int page_shift;   // log2(page_size)
 };
 
 struct SeqInfo {
@@ -82,22 +85,111 @@ __device__ __forceinline__ bool load_seq(const FwdParams& p, int b, SeqInfo& s) 
 // block table past the sequence's pages and always bring finite values.  A
 // page index outside the pool reads row 0 and is reported through the error
 // word.
-__device__ __forceinline__ int kv_row(const FwdParams& p, const SeqInfo& s, int b, int key,
-                                      int box) {
-  if (p.page_size <= 0) return s.k0 + key;
-  if (key >= s.lk) key = (s.lk - 1) - ((s.lk - 1) % box);
-  const int pg = __ldg(p.block_table + (size_t)b * p.max_pages + key / p.page_size);
+//
+// The block-table lookups go through a cursor owned by the one producer
+// thread, which walks keys in increasing order.  It keeps the key range of
+// the page in use and that page's base row, so a load inside the same page
+// costs two compares and an add; on entering a page it already fetches the
+// next page's entry, so that lookup's latency overlaps a page worth of loads
+// instead of stalling the next TMA issue.
+struct PageCursor {
+  int lo = 0, hi = 0;    // sequence keys [lo, hi) of the page in use
+  int base = 0;          // pool row of key lo, minus lo
+  int nxt_lp = -1, nxt_pp = 0;  // the following logical page and its pool page
+};
+
+__device__ __forceinline__ void page_enter(const FwdParams& p, const SeqInfo& s, int b, int key,
+                                        PageCursor& pc) {
+  const int lp = key >> p.page_shift;
+  const int* row = p.block_table + (size_t)b * p.max_pages;
+  int pg = lp == pc.nxt_lp ? pc.nxt_pp : __ldg(row + lp);
+  pc.nxt_lp = lp + 1;
+  pc.nxt_pp = (long long)(lp + 1) * p.page_size < s.lk ? __ldg(row + lp + 1) : 0;
   if (pg < 0 || (long long)(pg + 1) * p.page_size > p.total_k) {
     if (p.err) atomicCAS(p.err, 0, -6);
-    return 0;
+    pg = 0;
   }
-  return pg * p.page_size + (key & (p.page_size - 1));
+  pc.lo = lp << p.page_shift;
+  pc.hi = pc.lo + p.page_size;
+  pc.base = pg * p.page_size - pc.lo;
+}
+
+__device__ __forceinline__ int kv_row_walk(const FwdParams& p, const SeqInfo& s, int b, int key,
+                                           int box, PageCursor& pc) {
+  if (p.page_size <= 0) return s.k0 + key;
+  if (key >= s.lk) key = (s.lk - 1) & ~(box - 1);
+  if (__builtin_expect(key < pc.lo || key >= pc.hi, 0)) page_enter(p, s, b, key, pc);
+  return pc.base + key;
+}
+
+// ---- longest-first dispatch of decode tiles
+// The CTAs of a grid start roughly in linear block order (x fastest, then y,
+// then z).  A decode CTA's work is its split's share of one sequence's keys,
+// so in a varlen batch the grid order leaves long splits for the last wave
+// while the other SMs idle.  The CTA's linear index is therefore read as
+// (rank, split, KV head, row tile), rank slowest, where rank orders the
+// sequences by key count, longest first, ties by index: the launch becomes a
+// longest-processing-time-first list schedule of the splits.  The mapping is
+// a bijection onto the same (tile, sequence, head, split) set, so the
+// results do not change.  Larger batches keep the grid order.  (cutlass
+// "Adds variable sequence lengths to the Hopper CuTe DSL FMHA example",
+// section "Performance (GH200)": a static assignment over the max-length
+// grid balances skewed lengths poorly; a length-aware schedule is the named
+// follow-up.)
+constexpr int kMaxRankedSeqs = 128;
+
+struct TileIdx {
+  int m_blk, b, kh, split;
+};
+
+__device__ __forceinline__ int seq_keys(const FwdParams& p, int b) {
+  return p.page_size > 0 ? __ldg(p.seqlens_k + b) : __ldg(p.cu_k + b + 1) - __ldg(p.cu_k + b);
+}
+
+// Tile of this CTA in plain grid order: x = row tile, y = sequence * h_kv +
+// KV head, z = split.
+__device__ __forceinline__ TileIdx grid_order_tile(const FwdParams& p) {
+  TileIdx t;
+  t.m_blk = blockIdx.x;
+  t.b = blockIdx.y / p.h_kv;
+  t.kh = blockIdx.y - t.b * p.h_kv;
+  t.split = blockIdx.z;
+  return t;
+}
+
+// Every thread of the CTA calls this: it holds two barriers.  `keys` and
+// `pick` are shared-memory scratch of kMaxRankedSeqs ints and one int.
+__device__ __forceinline__ TileIdx longest_first_tile(const FwdParams& p, int* keys, int* pick) {
+  const int gx = gridDim.x;
+  const int ns = gridDim.z;
+  int v = blockIdx.x + gx * (blockIdx.y + gridDim.y * blockIdx.z);
+  TileIdx t;
+  t.m_blk = v % gx;
+  v /= gx;
+  t.kh = v % p.h_kv;
+  v /= p.h_kv;
+  t.split = v % ns;
+  const int rank = v / ns;
+  t.b = rank;
+  if (p.batch > 1 && p.batch <= kMaxRankedSeqs) {  // else the identity order
+    for (int i = threadIdx.x; i < p.batch; i += blockDim.x) keys[i] = seq_keys(p, i);
+    __syncthreads();
+    for (int i = threadIdx.x; i < p.batch; i += blockDim.x) {
+      const int li = keys[i];
+      int r = 0;
+      for (int c = 0; c < p.batch; ++c) r += (keys[c] > li) | ((keys[c] == li) & (c < i));
+      if (r == rank) *pick = i;
+    }
+    __syncthreads();
+    t.b = *pick;
+  }
+  return t;
 }
 
 // First key of a tile's load schedule: the split's first key, rounded down to
 // the load granularity in paged mode so no load crosses a page.
 __device__ __forceinline__ int load_base(const FwdParams& p, int k0, int granularity) {
-  return p.page_size > 0 ? k0 - (k0 % granularity) : k0;
+  return p.page_size > 0 ? k0 & ~(granularity - 1) : k0;
 }
 
 // Allowed keys [lo, hi) of query i in a (lq, lk) sequence: everything without

@@ -14,15 +14,24 @@ namespace fa {
 int simt_max_rows(int dtype, int d_qk, int d_v);
 
 // Launch the CUDA-core split kernel.  grid = (row tiles, batch*h_kv, ns).
-cudaError_t launch_simt(int dtype, int d_qk, int d_v, int rows_per_tile, const FwdParams& p,
-                        const CUtensorMap& tmK, const CUtensorMap& tmV, dim3 grid,
-                        cudaStream_t stream);
-cudaError_t launch_simt_bf16(int d_qk, int d_v, int rt, const FwdParams& p, const CUtensorMap& tmK,
-                             const CUtensorMap& tmV, dim3 grid, cudaStream_t stream);
-cudaError_t launch_simt_fp16(int d_qk, int d_v, int rt, const FwdParams& p, const CUtensorMap& tmK,
-                             const CUtensorMap& tmV, dim3 grid, cudaStream_t stream);
-cudaError_t launch_simt_e4m3(int d_qk, int d_v, int rt, const FwdParams& p, const CUtensorMap& tmK,
-                             const CUtensorMap& tmV, dim3 grid, cudaStream_t stream);
+// `ordered` dispatches the tiles longest sequence first.
+cudaError_t launch_simt(int dtype, int d_qk, int d_v, int rows_per_tile, bool ordered,
+                        const FwdParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                        dim3 grid, cudaStream_t stream);
+// One instantiation per (input type, order), each in its own translation unit.
+template <int DT, bool ORDERED>
+cudaError_t launch_simt_t(int d_qk, int d_v, int rt, const FwdParams& p, const CUtensorMap& tmK,
+                          const CUtensorMap& tmV, dim3 grid, cudaStream_t stream);
+#define FA_SIMT_INSTANCE(DT, ORD)                                                                \
+  template cudaError_t launch_simt_t<DT, ORD>(int, int, int, const FwdParams&, const CUtensorMap&, \
+                                              const CUtensorMap&, dim3, cudaStream_t)
+#define FA_SIMT_EXTERN(DT, ORD) extern FA_SIMT_INSTANCE(DT, ORD)
+FA_SIMT_EXTERN(kBF16, false);
+FA_SIMT_EXTERN(kBF16, true);
+FA_SIMT_EXTERN(kFP16, false);
+FA_SIMT_EXTERN(kFP16, true);
+FA_SIMT_EXTERN(kE4M3, false);
+FA_SIMT_EXTERN(kE4M3, true);
 
 // Launch the tcgen05 split kernel.  grid = (query tiles, batch*h_kv, ns).
 cudaError_t launch_umma(int dtype, int d_qk, int d_v, const FwdParams& p, const CUtensorMap& tmQ,

@@ -3,7 +3,8 @@
 // by the HBM stream of K and V, not by arithmetic, so it stays on the FP32
 // pipes and spends its effort on keeping bytes in flight.
 //
-// One CTA = one (row tile, sequence * KV head, split).  A producer warp
+// One CTA = one (row tile, sequence * KV head, split), dispatched longest
+// sequence first for varlen batches (longest_first_tile).  A producer warp
 // streams 32-key chunks of K and V for its KV head through an NS-stage ring
 // of 128B-swizzled shared-memory panels with TMA (cp.async.bulk.tensor), one
 // mbarrier pair per stage.  NW consumer warps take chunks round-robin; each
@@ -50,7 +51,8 @@ struct SimtCfg {
   static constexpr int OFF_MRG = OFF_PS + NW * RT * KC * 4;
   static constexpr int MRG_STRIDE = DV + 2;
   static constexpr int OFF_FLAG = OFF_MRG + NW * RT * MRG_STRIDE * 4;
-  static constexpr int SMEM = OFF_FLAG + 16 + 1024;     // + alignment slack
+  static constexpr int OFF_RANK = OFF_FLAG + 16;        // dispatch-order scratch
+  static constexpr int SMEM = OFF_RANK + (kMaxRankedSeqs + 4) * 4 + 1024;  // + alignment slack
   static_assert(DV % 32 == 0, "d_v must be a multiple of 32");
   static_assert(BPL == 2 || BPL == 4 || BPL == 8 || BPL == 16, "unsupported V lane width");
   static_assert(RT <= NW, "one epilogue warp per row");
@@ -77,7 +79,7 @@ __device__ __forceinline__ void lds_words(const uint8_t* p, uint32_t* w) {
   }
 }
 
-template <int DT, int DQK, int DV, int RT, int NW, int NS>
+template <int DT, int DQK, int DV, int RT, int NW, int NS, bool ORDERED>
 __global__ void __launch_bounds__((NW + 1) * 32)
     simt_splitkv_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV) {
@@ -90,12 +92,18 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int m_blk = blockIdx.x;
-  const int b = blockIdx.y / p.h_kv;
-  const int kh = blockIdx.y - b * p.h_kv;
-  const int split = blockIdx.z;
+  if (__syncthreads_or(timed_out_before(p.err))) return;
+  int* rank_scratch = reinterpret_cast<int*>(smem + C::OFF_RANK);
+  // The order is a compile-time choice: the kernel's decode loop is sensitive
+  // to the code around it, and the grid-order variant keeps single-sequence
+  // launches on the leanest code.
+  const TileIdx tile = ORDERED ? longest_first_tile(p, rank_scratch, rank_scratch + kMaxRankedSeqs)
+                               : grid_order_tile(p);
+  const int m_blk = tile.m_blk;
+  const int b = tile.b;
+  const int kh = tile.kh;
+  const int split = tile.split;
 
-  if (timed_out_before(p.err)) return;
   SeqInfo sq;
   if (!load_seq(p, b, sq)) {
     if (threadIdx.x == 0) record_error(p.err, kErrDeviceArg);
@@ -135,13 +143,14 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       const uint64_t pol = gridDim.x == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
+      PageCursor pages;
       for (int c = 0; c < nchunks; ++c) {
         const int st = c % NS;
+        const int row = kv_row_walk(p, sq, b, key0 + c * C::KC, C::KC, pages);
         if (c >= NS && !mbar_wait(bar_empty + 8 * st, ((c / NS) - 1) & 1, p.err, abort_flag)) break;
         const uint32_t dst = sbase + st * C::STAGE;
         const uint32_t fb = bar_full + 8 * st;
         mbar_arrive_expect_tx(fb, C::STAGE);
-        const int row = kv_row(p, sq, b, key0 + c * C::KC, C::KC);
 #pragma unroll
         for (int pk = 0; pk < C::NPK; ++pk)
           tma_load_3d(dst + pk * C::PANEL, &tmK, fb, pk * C::PANEL_ELEMS, kh, row, pol);

@@ -1,13 +1,8 @@
-// CUDA-core split kernel instantiations for e4m3 inputs.
+// CUDA-core split kernel instantiations for e4m3 inputs, tiles in grid order.
 #include "fa_simt_launch.cuh"
 
 namespace fa {
 
-cudaError_t launch_simt_e4m3(int d_qk, int d_v, int rt, const FwdParams& p, const CUtensorMap& tmK,
-                             const CUtensorMap& tmV, dim3 grid, cudaStream_t stream) {
-  if (d_qk == 128 && d_v == 128) return launch_simt_dims<kE4M3, 128, 128, 4>(rt, p, tmK, tmV, grid, stream);
-  if (d_qk == 192 && d_v == 128) return launch_simt_dims<kE4M3, 192, 128, 2>(rt, p, tmK, tmV, grid, stream);
-  return cudaErrorInvalidValue;
-}
+FA_SIMT_INSTANCE(kE4M3, false);
 
 }  // namespace fa

@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(384, 1)
   const int group = p.group;
   const int qpt = 128 / group;
 
-  if (timed_out_before(p.err)) return;
+  if (__syncthreads_or(timed_out_before(p.err))) return;
   SeqInfo sq;
   if (!load_seq(p, b, sq)) {
     if (threadIdx.x == 0) record_error(p.err, kErrDeviceArg);
@@ -183,32 +183,47 @@ __global__ void __launch_bounds__(384, 1)
           tma_load_3d(sbase + C::OFF_Q + (t * C::NPQ + pq) * C::PANEL, &tmQ, q_full,
                       pq * C::PANEL_ELEMS, kh * group, sq.q0 + q_start + t * qpt, pol_q);
       // K(0), K(1), V(0), K(2), V(1), ...: K one block ahead of V.
+      PageCursor pages_k, pages_v;
       for (int j = 0; j <= nblk; ++j) {
         if (j < nblk) {
           const int st = j % KS;
+          int rows[kMaxSub];  // rows resolved before the wait, off the refill's critical path
+#pragma unroll
+          for (int sb = 0; sb < kMaxSub; ++sb)
+            if (sb < nsub)
+              rows[sb] = kv_row_walk(p, sq, b, kb0 + j * kBlockN + sb * box_rows, box_rows,
+                                     pages_k);
           if (j >= KS && !mbar_wait(k_empty + 8 * st, ((j / KS) - 1) & 1, p.err, abort_flag)) break;
           const uint32_t dst = sbase + C::OFF_K + st * C::K_STAGE;
           mbar_arrive_expect_tx(k_full + 8 * st, C::K_STAGE);
 #pragma unroll
-          for (int pk = 0; pk < C::NPQ; ++pk)
-            for (int sb = 0; sb < nsub; ++sb)
-              tma_load_3d(dst + pk * C::PANEL + sb * box_rows * 128, &tmK, k_full + 8 * st,
-                          pk * C::PANEL_ELEMS, kh, kv_row(p, sq, b, kb0 + j * kBlockN + sb * box_rows, box_rows),
-                          pol_kv);
+          for (int sb = 0; sb < kMaxSub; ++sb)
+            if (sb < nsub)
+#pragma unroll
+              for (int pk = 0; pk < C::NPQ; ++pk)
+                tma_load_3d(dst + pk * C::PANEL + sb * box_rows * 128, &tmK, k_full + 8 * st,
+                            pk * C::PANEL_ELEMS, kh, rows[sb], pol_kv);
           issued_k = j + 1;
         }
         if (j >= 1) {
           const int jv = j - 1;
           const int st = jv % VS;
+          int rows[kMaxSub];  // rows resolved before the wait, off the refill's critical path
+#pragma unroll
+          for (int sb = 0; sb < kMaxSub; ++sb)
+            if (sb < nsub)
+              rows[sb] = kv_row_walk(p, sq, b, kb0 + jv * kBlockN + sb * box_rows, box_rows,
+                                     pages_v);
           if (jv >= VS && !mbar_wait(v_empty + 8 * st, ((jv / VS) - 1) & 1, p.err, abort_flag)) break;
           const uint32_t dst = sbase + C::OFF_V + st * C::V_STAGE;
           mbar_arrive_expect_tx(v_full + 8 * st, C::V_STAGE);
 #pragma unroll
-          for (int pv = 0; pv < C::NPV; ++pv)
-            for (int sb = 0; sb < nsub; ++sb)
-              tma_load_3d(dst + pv * C::PANEL + sb * box_rows * 128, &tmV, v_full + 8 * st,
-                          pv * C::PANEL_ELEMS, kh, kv_row(p, sq, b, kb0 + jv * kBlockN + sb * box_rows, box_rows),
-                          pol_kv);
+          for (int sb = 0; sb < kMaxSub; ++sb)
+            if (sb < nsub)
+#pragma unroll
+              for (int pv = 0; pv < C::NPV; ++pv)
+                tma_load_3d(dst + pv * C::PANEL + sb * box_rows * 128, &tmV, v_full + 8 * st,
+                            pv * C::PANEL_ELEMS, kh, rows[sb], pol_kv);
           issued_v = jv + 1;
         }
       }

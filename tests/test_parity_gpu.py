@@ -297,3 +297,18 @@ def test_head_dim_256(kernel, dtype, causal):
     out, lse = run_gpu(inp, causal=causal, num_splits=3, flags=kernel)
     o_ref, l_ref = reference(inp, 0.0, causal)
     assert_close(inp, out, lse, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("batch", [2, 128, 129])
+def test_longest_first_dispatch_batches(batch):
+    """Decode CTAs are dispatched longest sequence first for batches of 2 to
+    128 and in grid order beyond: both orders cover every (sequence, head,
+    split) once.  Lengths repeat (ties), include empty sequences and are not
+    sorted; the two query rows of a group stay on the CUDA-core kernel."""
+    rng = np.random.default_rng(batch)
+    lens_k = [int(x) for x in rng.choice([0, 1, 130, 200, 640], size=batch)]
+    lens_k[0] = 900
+    inp = make_inputs([1] * batch, lens_k, 4, 2, 64, 64, "bf16", seed=21)
+    out, lse = run_gpu(inp, num_splits=3, flags=fa.FA_KERNEL_SIMT)
+    o_ref, l_ref = reference(inp)
+    assert_close(inp, out, lse, o_ref, l_ref)

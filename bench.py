@@ -229,8 +229,8 @@ def measured_peaks():
 
 
 KERNEL_SOURCES = {
-    "simt_splitkv": ("fa_simt.cuh", "fa_simt_launch.cuh", "fa_simt_bf16.cu", "fa_common.cuh",
-                     "fa_ptx.cuh", "fa_convert.cuh"),
+    "simt_splitkv": ("fa_simt.cuh", "fa_simt_launch.cuh", "fa_simt_bf16.cu",
+                     "fa_simt_bf16_ordered.cu", "fa_common.cuh", "fa_ptx.cuh", "fa_convert.cuh"),
     "umma_splitkv": ("fa_umma.cuh", "fa_umma_launch.cuh", "fa_umma_bf16.cu", "fa_umma_e4m3.cu",
                      "fa_common.cuh", "fa_ptx.cuh", "fa_convert.cuh"),
     "umma2_splitkv": ("fa_umma2.cuh", "fa_umma2_launch.cuh", "fa_umma2_bf16.cu", "fa_common.cuh",

@@ -312,3 +312,32 @@ def test_longest_first_dispatch_batches(batch):
     out, lse = run_gpu(inp, num_splits=3, flags=fa.FA_KERNEL_SIMT)
     o_ref, l_ref = reference(inp)
     assert_close(inp, out, lse, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("kernel", [fa.FA_KERNEL_SIMT, fa.FA_KERNEL_UMMA])
+@pytest.mark.parametrize("mask", ["none", "causal", "window"])
+def test_fp8_edge_lengths_masks(kernel, mask):
+    """cutlass varlen page, "Tests": fp8 with the edge lengths (1, 0, 63, 64,
+    65, 128, 129, 700), GQA 8:2 and each mask; fp8 tolerance."""
+    lens = [1, 0, 63, 64, 65, 128, 129, 700]
+    inp = make_inputs(lens, lens, 8, 2, 128, 128, "e4m3", seed=31)
+    causal = mask == "causal"
+    wl = 128 if mask == "window" else -1
+    out, lse = run_gpu(inp, causal=causal, window_left=wl, num_splits=3, flags=kernel)
+    o_ref, l_ref = reference(inp, 0.0, causal, wl)
+    assert_close(inp, out, lse, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("varying", ["q", "k"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_one_side_only(kernel, varying, causal):
+    """cutlass varlen page, "Tests": variable-length Q only and K only (the
+    other side has one length for every sequence)."""
+    ragged = [5, 130, 1, 64, 257]
+    fixed = [96] * len(ragged)
+    lens_q, lens_k = (ragged, fixed) if varying == "q" else (fixed, ragged)
+    inp = make_inputs(lens_q, lens_k, 8, 2, 128, 128, "bf16", seed=32)
+    out, lse = run_gpu(inp, causal=causal, num_splits=2, flags=kernel)
+    o_ref, l_ref = reference(inp, 0.0, causal)
+    assert_close(inp, out, lse, o_ref, l_ref)

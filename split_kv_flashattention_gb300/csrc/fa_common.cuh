@@ -157,6 +157,28 @@ __device__ __forceinline__ TileIdx grid_order_tile(const FwdParams& p) {
   return t;
 }
 
+// Tile of a tensor-core CTA: grid x = query tiles, y = sequence * h_kv + KV
+// head, z = split.  Query tiles run last tile first.  Without a mask every
+// tile of a sequence does the same work, and the x-fastest order keeps the
+// tiles of one (sequence, head), which share K/V in L2, together.  With a
+// causal or window mask a tile's work grows with its index m and hardly
+// depends on the sequence, so the tiles run m-major (all sequences' last
+// tiles first): a longest-first order computed from the block index alone.
+__device__ __forceinline__ TileIdx query_tile_order(const FwdParams& p) {
+  TileIdx t;
+  int x = blockIdx.x, y = blockIdx.y;
+  if (p.causal || p.window_left >= 0) {
+    const int lin = x + gridDim.x * y;
+    x = lin / gridDim.y;
+    y = lin - x * gridDim.y;
+  }
+  t.m_blk = gridDim.x - 1 - x;
+  t.b = y / p.h_kv;
+  t.kh = y - t.b * p.h_kv;
+  t.split = blockIdx.z;
+  return t;
+}
+
 // Every thread of the CTA calls this: it holds two barriers.  `keys` and
 // `pick` are shared-memory scratch of kMaxRankedSeqs ints and one int.
 __device__ __forceinline__ TileIdx longest_first_tile(const FwdParams& p, int* keys, int* pick) {

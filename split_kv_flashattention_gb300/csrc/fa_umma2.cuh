@@ -91,10 +91,11 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int m_blk = gridDim.x - 1 - blockIdx.x;  // heaviest (latest) tiles first
-  const int b = blockIdx.y / p.h_kv;
-  const int kh = blockIdx.y - b * p.h_kv;
-  const int split = blockIdx.z;
+  const TileIdx tile = query_tile_order(p);  // heaviest (latest) tiles first
+  const int m_blk = tile.m_blk;
+  const int b = tile.b;
+  const int kh = tile.kh;
+  const int split = tile.split;
   const int group = p.group;
   const int qpt = 128 / group;
 

@@ -341,3 +341,20 @@ def test_varlen_one_side_only(kernel, varying, causal):
     out, lse = run_gpu(inp, causal=causal, num_splits=2, flags=kernel)
     o_ref, l_ref = reference(inp, 0.0, causal)
     assert_close(inp, out, lse, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("ns", [2, 4])
+@pytest.mark.parametrize("mask", ["causal", "window"])
+def test_two_tile_causal_splits_with_idle_first_tile(ns, mask):
+    """Two-tile kernel, causal/window with splits: in the later splits the
+    first tile of a pair sees no key (its rows end before the split starts)
+    while the second tile does; it must write the empty partial (O = 0,
+    LSE = -inf) and the combine must return the second tile's rows intact."""
+    lens = [200, 256, 300]
+    inp = make_inputs(lens, lens, 2, 2, 128, 128, "bf16", seed=33)
+    causal = mask == "causal"
+    wl = 100 if mask == "window" else -1
+    out, lse = run_gpu(inp, causal=causal, window_left=wl, num_splits=ns,
+                       flags=fa.FA_KERNEL_UMMA2)
+    o_ref, l_ref = reference(inp, 0.0, causal, wl)
+    assert_close(inp, out, lse, o_ref, l_ref)

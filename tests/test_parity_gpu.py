@@ -358,3 +358,32 @@ def test_two_tile_causal_splits_with_idle_first_tile(ns, mask):
                        flags=fa.FA_KERNEL_UMMA2)
     o_ref, l_ref = reference(inp, 0.0, causal, wl)
     assert_close(inp, out, lse, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("growth", ["moderate", "extreme"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_running_max_jumps_between_blocks(kernel, growth, causal):
+    """Keys scaled block by block so a row's score maximum jumps far past the
+    lazy-rescale threshold in later 128-key blocks (moderate: up to about 2^100
+    in exp2 units; extreme: past the fp32 exponent range if taken against the
+    old maximum).  Exercises the kernels' rescale paths, including the
+    two-tile kernel's recomputation of a block from the scores in TMEM."""
+    lens = [700, 300]
+    inp = make_inputs(lens, lens, 2, 2, 128, 128, "bf16", seed=34)
+    factors = [1.0, 1.0, 8.0, 8.0, 40.0, 1.0] if growth == "moderate" else [1.0, 200.0, 1.0, 1.0, 1.0, 1.0]
+    k = inp.k.float()
+    cu = inp.cu_seqlens_k.tolist()
+    for b in range(len(lens)):
+        for blk, f in enumerate(factors):
+            r0 = cu[b] + 128 * blk
+            r1 = min(cu[b + 1], r0 + 128)
+            if r0 < r1:
+                k[r0:r1] *= f
+    inp.k = k.to(inp.k.dtype)
+    # Such peaked rows give O close to one V row; V / 4 keeps |O| < 1, where
+    # rounding O to bf16 costs under 2^-9 of the 1e-2 tolerance.
+    inp.v = (inp.v.float() * 0.25).to(inp.v.dtype)
+    out, lse = run_gpu(inp, causal=causal, num_splits=1, flags=kernel)
+    o_ref, l_ref = reference(inp, 0.0, causal)
+    assert_close(inp, out, lse, o_ref, l_ref)

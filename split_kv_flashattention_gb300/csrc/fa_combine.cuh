@@ -3,7 +3,8 @@
 // aiter PR "[FlyDSL] Enable FP8 FMHA split-K for short cached-prefix
 // queries": the timed unit is "attention and split combine", with a per-call
 // fp32 workspace.  For every output row (token t, head h) one warp reads the
-// ns partial LSEs (lanes take splits s, s+32, ...), forms
+// ns partial LSEs (lanes take splits s, s+32, ...) together with the partial
+// O rows (one round of loads for up to 16 splits), forms
 //     M = max_s lse_s,  w_s = exp(lse_s - M),  LSE = M + ln(sum_s w_s)
 // and accumulates O = sum_s (w_s / sum w) * O_s with 128-bit loads, lane l
 // owning columns [l*d_v/32, (l+1)*d_v/32).  Rows whose splits are all empty
@@ -21,34 +22,66 @@ namespace fa {
 template <int DV>
 __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ FwdParams p) {
   constexpr int DPL = DV / 32;
-  // Launched as a programmatic dependent of the partial kernel: wait for its
-  // partials before reading them.
-  pdl_wait();
+  constexpr int CH = DPL >= 8 ? 8 : 16;  // partial O rows loaded per round
   const int lane = threadIdx.x & 31;
   const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (gw >= (long long)p.slots * p.h_q) return;
-  const int slot = (int)(gw / p.h_q);
-  const int h = (int)(gw - (long long)slot * p.h_q);
+  const bool in_grid = gw < (long long)p.slots * p.h_q;
+  const int slot = in_grid ? (int)(gw / p.h_q) : 0;
+  const int h = in_grid ? (int)(gw - (long long)slot * p.h_q) : 0;
   const int b = slot / p.max_seqlen_q;
   const int i = slot - b * p.max_seqlen_q;
+  // The sequence offsets do not come from the partial kernel: read them
+  // before waiting for it (programmatic dependent launch).
   SeqInfo sq;
-  if (!load_seq(p, b, sq)) return;  // reported by the partial kernel
-  if (i >= sq.lq) return;
+  const bool valid = in_grid && load_seq(p, b, sq) && i < sq.lq;  // bad offsets: reported by the partial kernel
+  pdl_wait();
+  if (!valid) return;
   const int t = sq.q0 + i;
   const int ns = p.num_splits;
   const size_t split_stride = (size_t)p.slots * p.h_q;
   const size_t row0 = (size_t)slot * p.h_q + h;
+  const float* obase = p.ws_o + row0 * DV + lane * DPL;
+  const size_t ostride = split_stride * DV;
 
-  constexpr float kLog2e = 1.4426950408889634f;
-  constexpr float kLn2 = 0.69314718055994531f;
+  // One round of loads: every partial LSE (lane l holds splits l, l+32, ...)
+  // and the first CH partial O rows.  Splits past a sequence's key range were
+  // written as O = 0, LSE = -inf, so every split below ns is readable.
+  auto load_o = [&](int s, float* v) {
+    const float* src = obase + (size_t)s * ostride;
+    if constexpr (DPL % 4 == 0) {
+#pragma unroll
+      for (int e = 0; e < DPL; e += 4) {
+        const float4 q = __ldg(reinterpret_cast<const float4*>(src + e));
+        v[e] = q.x;
+        v[e + 1] = q.y;
+        v[e + 2] = q.z;
+        v[e + 3] = q.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < DPL; e += 2) {
+        const float2 q = __ldg(reinterpret_cast<const float2*>(src + e));
+        v[e] = q.x;
+        v[e + 1] = q.y;
+      }
+    }
+  };
+  float ov[CH][DPL];
+#pragma unroll
+  for (int c = 0; c < CH; ++c)
+    if (c < ns) load_o(c, ov[c]);
   float lv[kMaxSplits / 32];
-  float M = -CUDART_INF_F;
 #pragma unroll
   for (int u = 0; u < kMaxSplits / 32; ++u) {
     const int s = u * 32 + lane;
     lv[u] = s < ns ? __ldg(p.ws_l + s * split_stride + row0) : -CUDART_INF_F;
-    M = fmaxf(M, lv[u]);
   }
+
+  constexpr float kLog2e = 1.4426950408889634f;
+  constexpr float kLn2 = 0.69314718055994531f;
+  float M = -CUDART_INF_F;
+#pragma unroll
+  for (int u = 0; u < kMaxSplits / 32; ++u) M = fmaxf(M, lv[u]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
 
@@ -68,33 +101,24 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ Fw
     for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
     const float inv = 1.f / L;
     lse_out = M + __log2f(L) * kLn2;
-    const float* base = p.ws_o + row0 * DV + lane * DPL;
 #pragma unroll
-    for (int u = 0; u < kMaxSplits / 32; ++u) {
-      if (u * 32 >= ns) break;
-      const float wu = w[u] * inv;
-      const int n_here = min(32, ns - u * 32);
-#pragma unroll 4
-      for (int sl = 0; sl < n_here; ++sl) {
-        const float ws = __shfl_sync(0xffffffffu, wu, sl);
-        const float* src = base + (size_t)(u * 32 + sl) * split_stride * DV;
-        if (ws != 0.f) {
-          if constexpr (DPL % 4 == 0) {
+    for (int u = 0; u < kMaxSplits / 32; ++u) w[u] *= inv;
+    for (int s0 = 0; s0 < ns; s0 += CH) {
+      if (s0 > 0) {
 #pragma unroll
-            for (int e = 0; e < DPL; e += 4) {
-              const float4 v = __ldg(reinterpret_cast<const float4*>(src + e));
-              acc[e] = fmaf(ws, v.x, acc[e]);
-              acc[e + 1] = fmaf(ws, v.y, acc[e + 1]);
-              acc[e + 2] = fmaf(ws, v.z, acc[e + 2]);
-              acc[e + 3] = fmaf(ws, v.w, acc[e + 3]);
-            }
-          } else {
+        for (int c = 0; c < CH; ++c)
+          if (s0 + c < ns) load_o(s0 + c, ov[c]);
+      }
 #pragma unroll
-            for (int e = 0; e < DPL; e += 2) {
-              const float2 v = __ldg(reinterpret_cast<const float2*>(src + e));
-              acc[e] = fmaf(ws, v.x, acc[e]);
-              acc[e + 1] = fmaf(ws, v.y, acc[e + 1]);
-            }
+      for (int c = 0; c < CH; ++c) {
+        const int s = s0 + c;
+        if (s < ns) {
+          const int u = s >> 5;
+          const float wu = u == 0 ? w[0] : u == 1 ? w[1] : u == 2 ? w[2] : w[3];
+          const float ws = __shfl_sync(0xffffffffu, wu, s & 31);
+          if (ws != 0.f) {
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc[e] = fmaf(ws, ov[c][e], acc[e]);
           }
         }
       }

@@ -349,7 +349,10 @@ __global__ void __launch_bounds__(192, 1)
     const bool warp_active = quarter * 32 < nrows;
     const int i = q_start + r / group;
     const int h = kh * group + (r - (r / group) * group);
-    int lo = 0, hi = 0;
+    // Rows outside the tile (past the sequence's queries, or beyond the
+    // group's heads) are never stored: they take an unbounded key range so
+    // that they never ask for masking, keeping every warp on one path.
+    int lo = -(1 << 30), hi = 1 << 30;
     if (row_ok) {
       row_key_range(i, sq.lq, sq.lk, p.causal, p.window_left, lo, hi);
       lo = max(lo, k0);
@@ -377,7 +380,9 @@ __global__ void __launch_bounds__(192, 1)
         float mx[8];
 #pragma unroll
         for (int t = 0; t < 8; ++t) mx[t] = -CUDART_INF_F;
-        if (!(kb >= lo && kb + kBlockN <= hi)) {
+        // Masking is decided for the whole warp (a lane-divergent branch
+        // here would split the warp for the rest of the block).
+        if (__any_sync(0xffffffffu, !(kb >= lo && kb + kBlockN <= hi))) {
 #pragma unroll
           for (int c = 0; c < 128; ++c) {
             const int key = kb + c;

@@ -312,7 +312,10 @@ __global__ void __launch_bounds__(384, 1)
     const bool row_ok = r < nrows;
     const int i = q_start + t * qpt + r / group;
     const int h = kh * group + (r - (r / group) * group);
-    int lo = 0, hi = 0;
+    // Rows outside the tile (past the sequence's queries, or beyond the
+    // group's heads) are never stored: they take an unbounded key range so
+    // that they never ask for masking, keeping every warp on one path.
+    int lo = -(1 << 30), hi = 1 << 30;
     if (row_ok) {
       row_key_range(i, sq.lq, sq.lk, p.causal, p.window_left, lo, hi);
       lo = max(lo, k0);
@@ -336,7 +339,9 @@ __global__ void __launch_bounds__(384, 1)
         const int kb = kb0 + j * kBlockN;
         float s[128];
         tmem_ld128(s_addr, reinterpret_cast<uint32_t*>(s));
-        if (!(kb >= lo && kb + kBlockN <= hi)) {
+        // Masking is decided for the whole warp (a lane-divergent branch
+        // here would split the warp for the rest of the block).
+        if (__any_sync(0xffffffffu, !(kb >= lo && kb + kBlockN <= hi))) {
 #pragma unroll
           for (int c = 0; c < 128; ++c) {
             const int key = kb + c;

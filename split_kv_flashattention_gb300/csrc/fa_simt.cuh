@@ -92,7 +92,10 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  if (__syncthreads_or(timed_out_before(p.err))) return;
+  if (threadIdx.x == 0) {  // descriptors fetched while the prologue runs
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
   int* rank_scratch = reinterpret_cast<int*>(smem + C::OFF_RANK);
   // The order is a compile-time choice: the kernel's decode loop is sensitive
   // to the code around it, and the grid-order variant keeps single-sequence
@@ -104,8 +107,12 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   const int kh = tile.kh;
   const int split = tile.split;
 
+  // The sequence offsets are loaded before the error-word check so that both
+  // reads share one memory latency.
   SeqInfo sq;
-  if (!load_seq(p, b, sq)) {
+  const bool seq_ok = load_seq(p, b, sq);
+  if (__syncthreads_or(timed_out_before(p.err))) return;
+  if (!seq_ok) {
     if (threadIdx.x == 0) record_error(p.err, kErrDeviceArg);
     return;
   }
@@ -140,8 +147,6 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   if (warp == NW) {
     // ---------------------------------------------------------- producer
     if (lane == 0 && nchunks > 0) {
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
       const uint64_t pol = gridDim.x == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
       PageCursor pages;
       for (int c = 0; c < nchunks; ++c) {

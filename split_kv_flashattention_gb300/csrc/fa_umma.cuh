@@ -157,9 +157,17 @@ __global__ void __launch_bounds__(192, 1)
   const int group = p.group;
   const int qpt = 128 / group;  // queries per tile
 
-  if (__syncthreads_or(timed_out_before(p.err))) return;
+  if (threadIdx.x == 0) {  // descriptors fetched while the prologue runs
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  // The sequence offsets are loaded before the error-word check so that both
+  // reads share one memory latency.
   SeqInfo sq;
-  if (!load_seq(p, b, sq)) {
+  const bool seq_ok = load_seq(p, b, sq);
+  if (__syncthreads_or(timed_out_before(p.err))) return;
+  if (!seq_ok) {
     if (threadIdx.x == 0) record_error(p.err, kErrDeviceArg);
     return;
   }
@@ -221,9 +229,6 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0) {
     // -------------------------------------------------------------- producer
     if (lane == 0 && nblk > 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
       const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = gridDim.x == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
       mbar_arrive_expect_tx(q_full, C::NPQ * qpt * group * 128);

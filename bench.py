@@ -233,6 +233,8 @@ KERNEL_SOURCES = {
                      "fa_simt_bf16_ordered.cu", "fa_common.cuh", "fa_ptx.cuh", "fa_convert.cuh"),
     "umma_splitkv": ("fa_umma.cuh", "fa_umma_launch.cuh", "fa_umma_bf16.cu", "fa_umma_e4m3.cu",
                      "fa_common.cuh", "fa_ptx.cuh", "fa_convert.cuh"),
+    "umma2p_splitkv": ("fa_umma2p.cuh", "fa_umma2p_launch.cuh", "fa_umma2p_bf16.cu", "fa_umma2.cuh",
+                       "fa_common.cuh", "fa_ptx.cuh", "fa_convert.cuh"),
     "umma2_splitkv": ("fa_umma2.cuh", "fa_umma2_launch.cuh", "fa_umma2_bf16.cu", "fa_common.cuh",
                       "fa_ptx.cuh", "fa_convert.cuh"),
 }
@@ -445,7 +447,12 @@ def main():
         if rows <= simt_rows:
             kern_tag = "simt_splitkv"
         elif rows > 128 and inp.dtype != "e4m3" and inp.d_qk <= 128:
-            kern_tag = "umma2_splitkv"
+            # the persistent form: one split, packed K/V, no mask, tile list fits
+            qpt = 128 // (inp.h_q // inp.h_kv)
+            pairs = -(-inp.max_seqlen_q // (2 * qpt))
+            persistent = (ns == 1 and not paged and not causal and inp.batch <= 128
+                          and pairs <= 512 and inp.batch * pairs <= 640)
+            kern_tag = "umma2p_splitkv" if persistent else "umma2_splitkv"
         else:
             kern_tag = "umma_splitkv"
     else:

@@ -427,9 +427,29 @@ int fwd_impl(const void* q, const void* k, const void* v, const int* cu_seqlens_
       CUtensorMap tmQ;
       st = make_tmap_3d(&tmQ, q, in_dtype, d_qk, h_q, total_q, qpt, p.group);
       if (st != FA_OK) return st;
-      dim3 grid((unsigned)ceil_div(max_seqlen_q, 2 * qpt), (unsigned)(batch * h_kv), (unsigned)ns);
-      e = in_dtype == kFP16 ? launch_umma2_fp16(d_qk, d_v, p, tmQ, tmK, tmV, grid, s)
-                            : launch_umma2_bf16(d_qk, d_v, p, tmQ, tmK, tmV, grid, s);
+      // One split over packed K/V without a mask, chosen automatically: the
+      // persistent form walks a tile list held in shared memory, so the batch
+      // and its query pairs must fit that list.  Under a causal or window
+      // mask the tiles are short and unequal, and the non-persistent grid
+      // (dispatched m-major by the hardware's own greedy scheduler) measured
+      // faster than the persistent kernel's static deal.
+      const long long pairs = ceil_div(max_seqlen_q, 2 * qpt);
+      const bool persistent = kernel_sel == FA_KERNEL_AUTO && ns == 1 && !paged && !causal &&
+                              window_left < 0 && batch <= 128 && pairs <= kMaxUnitPairs &&
+                              (long long)batch * pairs <= kMaxUnits;
+      if (persistent) {
+        int sms = 0;
+        st = device_sms(&sms);
+        if (st != FA_OK) return st;
+        const long long tiles = (long long)batch * pairs * h_kv;
+        dim3 grid((unsigned)(tiles < sms ? tiles : sms), 1, 1);
+        e = in_dtype == kFP16 ? launch_umma2p_fp16(d_qk, d_v, p, tmQ, tmK, tmV, grid, s)
+                              : launch_umma2p_bf16(d_qk, d_v, p, tmQ, tmK, tmV, grid, s);
+      } else {
+        dim3 grid((unsigned)ceil_div(max_seqlen_q, 2 * qpt), (unsigned)(batch * h_kv), (unsigned)ns);
+        e = in_dtype == kFP16 ? launch_umma2_fp16(d_qk, d_v, p, tmQ, tmK, tmV, grid, s)
+                              : launch_umma2_bf16(d_qk, d_v, p, tmQ, tmK, tmV, grid, s);
+      }
     } else if (use_umma) {
       const int qpt = 128 / p.group;
       p.tile_rows = qpt * p.group;

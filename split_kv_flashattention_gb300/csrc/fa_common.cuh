@@ -15,6 +15,10 @@ namespace fa {
 
 constexpr int kBlockN = 128;    // keys per split block
 constexpr int kMaxSplits = 128;
+// Tile list of the persistent two-tile kernel: (sequence, 256-row query pair)
+// units held in shared memory, 7 bits of sequence and 9 of pair each.
+constexpr int kMaxUnits = 640;
+constexpr int kMaxUnitPairs = 512;
 constexpr int kMinPage = 32;                 // smallest page of a paged K/V cache
 constexpr int kMaxSub = kBlockN / kMinPage;  // page-sized loads per key block, at most
 

@@ -56,6 +56,15 @@ cudaError_t launch_umma2_fp16(int d_qk, int d_v, const FwdParams& p, const CUten
                               const CUtensorMap& tmK, const CUtensorMap& tmV, dim3 grid,
                               cudaStream_t stream);
 
+// Launch the persistent two-tile kernel (one split, packed K/V, at most 128
+// sequences and kMaxUnits (sequence, query pair) units).  grid = (CTAs, 1, 1).
+cudaError_t launch_umma2p_bf16(int d_qk, int d_v, const FwdParams& p, const CUtensorMap& tmQ,
+                               const CUtensorMap& tmK, const CUtensorMap& tmV, dim3 grid,
+                               cudaStream_t stream);
+cudaError_t launch_umma2p_fp16(int d_qk, int d_v, const FwdParams& p, const CUtensorMap& tmQ,
+                               const CUtensorMap& tmK, const CUtensorMap& tmV, dim3 grid,
+                               cudaStream_t stream);
+
 // Launch the split combine (one warp per output row).
 cudaError_t launch_combine(const FwdParams& p, cudaStream_t stream);
 

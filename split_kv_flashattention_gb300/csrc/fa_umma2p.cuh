@@ -1,0 +1,582 @@
+// Persistent form of the two-tile tensor-core kernel, for one-split prefill.
+//
+// The non-persistent kernel pays, per 256-row query tile pair, a prologue
+// (offsets, barriers, TMEM allocation, then the latency of Q and the first K
+// block) and an epilogue (O out of TMEM) during which the tensor core idles;
+// across a varlen prefill that was about a seventh of each CTA's life.  Here
+// one CTA per SM walks a list of tiles: the next tile's Q and K/V are loaded
+// while the current tile's last blocks and epilogue run, and the TMEM
+// allocation, barriers and descriptors are set up once.
+//
+// cutlass "Adds variable sequence lengths to the Hopper CuTe DSL FMHA
+// example", section "Performance (GH200)": a persistent kernel that assigns
+// the max-length grid round-robin balances skewed lengths poorly, and a
+// length-aware schedule is the named follow-up.  This one first compacts the
+// tiles that exist (sequence, 256-row query pair) into a list ordered
+// longest first -- by key count without a mask, by query-pair index (the
+// causal work) with one -- and deals it out to the CTAs in snake order.
+//
+// Per tile everything is as in the two-tile kernel (fa_umma2.cuh): two
+// 128-row query tiles A and B share each K/V block, the MMA warp alternates
+// PV_A(j) S_A(j+1) PV_B(j) S_B(j+1), and the softmax warpgroups run the same
+// block body.  Across tiles the K/V rings, the S buffers and every barrier
+// keep running phase counts; two barriers are added: q_empty (the MMA warp's
+// commit after a tile's last S MMAs, so the producer may load the next Q) and
+// o_free[t] (the softmax warps' arrival once they have read a tile's O out of
+// TMEM, so the next tile's first PV may overwrite it).
+#pragma once
+
+#include <cuda.h>
+#include <math_constants.h>
+
+#include "fa_common.cuh"
+#include "fa_convert.cuh"
+#include "fa_ptx.cuh"
+#include "fa_umma2.cuh"
+
+namespace fa {
+
+template <int DT, int DQK, int DV, int KS, int VS>
+struct Umma2pCfg {
+  using B = Umma2Cfg<DT, DQK, DV, KS, VS>;
+  // Shared layout of the two-tile kernel, then: q_empty, o_free[2], the
+  // unit count and the unit list (b | m << 7, uint16).
+  static constexpr int OFF_BAR2 = B::OFF_FLAG + 16;
+  static constexpr int OFF_NUNITS = OFF_BAR2 + 24;
+  static constexpr int OFF_UNITS = OFF_NUNITS + 8;
+  static constexpr int SMEM = OFF_UNITS + 2 * kMaxUnits + 1024;
+  // Register split (launch: 384 x 168): the producer and MMA roles carry the
+  // tile walk (72 per thread), the softmax warpgroups keep a whole S row
+  // (216): 128*72 + 256*216 = 64512.
+  static constexpr int REGS_CTRL = 72;
+  static constexpr int REGS_SOFTMAX = 216;
+  static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX <= 384 * 168, "register split");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+  // Scratch for building the list (the K ring, before any load).
+  static constexpr int OFF_SCRATCH = B::OFF_K;
+  static_assert(KS * B::K_STAGE >= 4 * 129 * 4, "list scratch");
+};
+
+// Tile k of this CTA in the compacted list (snake order over the CTAs), or -1.
+__device__ __forceinline__ int unit_tile(int k, int n_tiles) {
+  const int G = gridDim.x;
+  const int c = blockIdx.x;
+  const int r = k * G + ((k & 1) ? (G - 1 - c) : c);
+  return r < n_tiles ? r : -1;
+}
+
+// Everything about one tile that every role needs, computed the same way by
+// each of them.
+struct PTile {
+  int b, kh, m_blk;
+  SeqInfo sq;
+  int q_start, nq_a, nq_b;
+  int k0, k1, kb0, nblk;
+};
+
+__device__ __forceinline__ void decode_ptile(const FwdParams& p, const uint16_t* units, int r,
+                                             int qpt, PTile& t) {
+  const int u = units[r / p.h_kv];
+  t.kh = r - (r / p.h_kv) * p.h_kv;
+  t.b = u & 127;
+  t.m_blk = u >> 7;
+  load_seq(p, t.b, t.sq);  // validated when the list was built
+  t.q_start = t.m_blk * 2 * qpt;
+  t.nq_a = min(qpt, t.sq.lq - t.q_start);
+  t.nq_b = max(0, min(qpt, t.sq.lq - t.q_start - qpt));
+  tile_split_range(t.q_start, t.q_start + t.nq_a + t.nq_b - 1, t.sq.lq, t.sq.lk, p.causal,
+                   p.window_left, 1, 0, t.k0, t.k1);
+  t.kb0 = t.k0;
+  t.nblk = t.k1 > t.k0 ? (t.k1 - t.kb0 + kBlockN - 1) / kBlockN : 0;
+}
+
+template <int DT, int DQK, int DV, int KS, int VS>
+__global__ void __launch_bounds__(384, 1)
+    umma2p_splitkv_kernel(const __grid_constant__ FwdParams p,
+                          const __grid_constant__ CUtensorMap tmQ,
+                          const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV) {
+  using C = Umma2Cfg<DT, DQK, DV, KS, VS>;
+  using CP = Umma2pCfg<DT, DQK, DV, KS, VS>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t pad = ((raw_u32 + 1023u) & ~1023u) - raw_u32;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw_u32 + pad;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int group = p.group;
+  const int qpt = 128 / group;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (__syncthreads_or(timed_out_before(p.err))) return;
+
+  // ---- the tile list: units (sequence, query pair) that exist, longest first
+  uint16_t* units = reinterpret_cast<uint16_t*>(smem + CP::OFF_UNITS);
+  int* n_units_s = reinterpret_cast<int*>(smem + CP::OFF_NUNITS);
+  {
+    int* s_pairs = reinterpret_cast<int*>(smem + CP::OFF_SCRATCH);  // [128]
+    int* s_keys = s_pairs + 128;                                     // [128]
+    int* s_order = s_keys + 128;                                     // [128] rank -> sequence
+    int* s_off = s_order + 128;                                      // [129]
+    for (int bb = threadIdx.x; bb < p.batch; bb += blockDim.x) {
+      SeqInfo s;
+      int pr = 0, key = 0;
+      if (load_seq(p, bb, s)) {
+        pr = min((s.lq + 2 * qpt - 1) / (2 * qpt), kMaxUnitPairs);
+        key = s.lk;
+      } else if (blockIdx.x == 0) {
+        record_error(p.err, kErrDeviceArg);
+      }
+      s_pairs[bb] = pr;
+      s_keys[bb] = key;
+    }
+    __syncthreads();
+    const bool masked = p.causal || p.window_left >= 0;
+    if (!masked) {
+      // sequences by key count, longest first (ties by index)
+      for (int bb = threadIdx.x; bb < p.batch; bb += blockDim.x) {
+        int rk = 0;
+        for (int c = 0; c < p.batch; ++c)
+          rk += (s_keys[c] > s_keys[bb]) | ((s_keys[c] == s_keys[bb]) & (c < bb));
+        s_order[rk] = bb;
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int acc = 0;
+        for (int rk = 0; rk < p.batch; ++rk) {
+          s_off[rk] = acc;
+          acc += s_pairs[s_order[rk]];
+        }
+        s_off[p.batch] = acc;
+        *n_units_s = min(acc, kMaxUnits);
+      }
+      __syncthreads();
+      for (int rk = threadIdx.x; rk < p.batch; rk += blockDim.x) {
+        const int bb = s_order[rk];
+        const int pr = s_pairs[bb];
+        for (int m = 0; m < pr; ++m) {
+          const int at = s_off[rk] + m;
+          if (at < kMaxUnits) units[at] = (uint16_t)(bb | ((pr - 1 - m) << 7));
+        }
+      }
+    } else if (warp == 0) {
+      // query pairs from the last (most keys under the mask) down, sequences
+      // in order within a level
+      int maxp = 0;
+      for (int bb = lane; bb < p.batch; bb += 32) maxp = max(maxp, s_pairs[bb]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) maxp = max(maxp, __shfl_xor_sync(0xffffffffu, maxp, o));
+      int n = 0;
+      for (int m = maxp - 1; m >= 0; --m) {
+        for (int base = 0; base < p.batch; base += 32) {
+          const int bb = base + lane;
+          const bool on = bb < p.batch && s_pairs[bb] > m;
+          const unsigned bal = __ballot_sync(0xffffffffu, on);
+          const int at = n + __popc(bal & ((1u << lane) - 1u));
+          if (on && at < kMaxUnits) units[at] = (uint16_t)(bb | (m << 7));
+          n += __popc(bal);
+        }
+      }
+      if (lane == 0) *n_units_s = min(n, kMaxUnits);
+    }
+  }
+
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  const uint32_t q_full = bar0;
+  const uint32_t k_full = bar0 + 8;                // [KS]
+  const uint32_t k_empty = k_full + 8 * KS;         // [KS]
+  const uint32_t v_full = k_empty + 8 * KS;         // [VS]
+  const uint32_t v_empty = v_full + 8 * VS;         // [VS]
+  const uint32_t s_full = v_empty + 8 * VS;         // [2]
+  const uint32_t p_ready = s_full + 16;            // [2]
+  const uint32_t o_done = p_ready + 16;            // [2]
+  const uint32_t drain = o_done + 16;
+  const uint32_t q_empty = sbase + CP::OFF_BAR2;
+  const uint32_t o_free = q_empty + 8;              // [2]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(k_full + 8 * s, 1);
+      mbar_init(k_empty + 8 * s, 1);
+    }
+    for (int s = 0; s < VS; ++s) {
+      mbar_init(v_full + 8 * s, 1);
+      mbar_init(v_empty + 8 * s, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(s_full + 8 * t, 1);
+      mbar_init(p_ready + 8 * t, 128);
+      mbar_init(o_done + 8 * t, 1);
+      mbar_init(o_free + 8 * t, 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + C::OFF_TMEM_SLOT, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();  // also publishes the tile list (and frees the scratch)
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int n_tiles = *n_units_s * p.h_kv;
+
+  if (warp < 4) {
+    regs_dec<CP::REGS_CTRL>();
+    int issued_k = 0, issued_v = 0, issued_q = 0;
+
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        const uint64_t pol_q = l2_policy_evict_first();
+        const uint64_t pol_kv = l2_policy_evict_last();
+        bool ok = true;
+        // K block j of tile T into the ring (false if the wait gave up).
+        auto load_k = [&](const PTile& T, int j) {
+          const int st = issued_k % KS;
+          if (issued_k >= KS &&
+              !mbar_wait(k_empty + 8 * st, ((issued_k / KS) - 1) & 1, p.err, abort_flag))
+            return false;
+          const uint32_t dst = sbase + C::OFF_K + st * C::K_STAGE;
+          mbar_arrive_expect_tx(k_full + 8 * st, C::K_STAGE);
+#pragma unroll
+          for (int pk = 0; pk < C::NPQ; ++pk)
+            tma_load_3d(dst + pk * C::PANEL, &tmK, k_full + 8 * st, pk * C::PANEL_ELEMS, T.kh,
+                        T.sq.k0 + T.kb0 + j * kBlockN, pol_kv);
+          ++issued_k;
+          return true;
+        };
+        auto load_v = [&](const PTile& T, int j) {
+          const int st = issued_v % VS;
+          if (issued_v >= VS &&
+              !mbar_wait(v_empty + 8 * st, ((issued_v / VS) - 1) & 1, p.err, abort_flag))
+            return false;
+          const uint32_t dst = sbase + C::OFF_V + st * C::V_STAGE;
+          mbar_arrive_expect_tx(v_full + 8 * st, C::V_STAGE);
+#pragma unroll
+          for (int pv = 0; pv < C::NPV; ++pv)
+            tma_load_3d(dst + pv * C::PANEL, &tmV, v_full + 8 * st, pv * C::PANEL_ELEMS, T.kh,
+                        T.sq.k0 + T.kb0 + j * kBlockN, pol_kv);
+          ++issued_v;
+          return true;
+        };
+        // Q and the first K/V block of a tile into L2, a tile ahead: the
+        // tile's own Q load can only start once the previous tile's last S
+        // MMAs have read the old Q, and then finds it in L2.
+        auto prefetch_tile = [&](const PTile& T) {
+          const int ntiles = T.nq_b > 0 ? 2 : 1;
+          for (int t = 0; t < ntiles; ++t)
+#pragma unroll
+            for (int pq = 0; pq < C::NPQ; ++pq)
+              tma_prefetch_l2_3d(&tmQ, pq * C::PANEL_ELEMS, T.kh * group, T.sq.q0 + T.q_start + t * qpt);
+#pragma unroll
+          for (int pk = 0; pk < C::NPQ; ++pk)
+            tma_prefetch_l2_3d(&tmK, pk * C::PANEL_ELEMS, T.kh, T.sq.k0 + T.kb0);
+#pragma unroll
+          for (int pv = 0; pv < C::NPV; ++pv)
+            tma_prefetch_l2_3d(&tmV, pv * C::PANEL_ELEMS, T.kh, T.sq.k0 + T.kb0);
+        };
+        for (int k = 0; ok; ++k) {
+          const int r = unit_tile(k, n_tiles);
+          if (r < 0) break;
+          PTile T;
+          decode_ptile(p, units, r, qpt, T);
+          if (T.nblk == 0) continue;
+          {  // the next tile with work, prefetched into L2
+            for (int k2 = k + 1;; ++k2) {
+              const int r2 = unit_tile(k2, n_tiles);
+              if (r2 < 0) break;
+              PTile T2;
+              decode_ptile(p, units, r2, qpt, T2);
+              if (T2.nblk == 0) continue;
+              prefetch_tile(T2);
+              break;
+            }
+          }
+          // K(0) first: its ring stage frees long before the old Q does
+          if (!load_k(T, 0)) break;
+          // Q of this tile once the previous tile's S MMAs have read theirs
+          if (issued_q > 0 && !mbar_wait(q_empty, (issued_q - 1) & 1, p.err, abort_flag)) break;
+          const int ntiles = T.nq_b > 0 ? 2 : 1;
+          mbar_arrive_expect_tx(q_full, ntiles * C::NPQ * qpt * group * 128);
+          for (int t = 0; t < ntiles; ++t)
+#pragma unroll
+            for (int pq = 0; pq < C::NPQ; ++pq)
+              tma_load_3d(sbase + C::OFF_Q + (t * C::NPQ + pq) * C::PANEL, &tmQ, q_full,
+                          pq * C::PANEL_ELEMS, T.kh * group, T.sq.q0 + T.q_start + t * qpt, pol_q);
+          ++issued_q;
+          // K(1), V(0), K(2), V(1), ...: K one block ahead of V.
+          for (int j = 1; j <= T.nblk; ++j) {
+            if (j < T.nblk && !load_k(T, j)) {
+              ok = false;
+              break;
+            }
+            if (!load_v(T, j - 1)) {
+              ok = false;
+              break;
+            }
+          }
+        }
+      }
+    } else if (warp == 1) {
+      // ---------------------------------------------------------------- MMA
+      if (lane == 0) {
+        auto issue_s = [&](int t, int kst) {
+          const uint32_t q_addr = sbase + C::OFF_Q + t * C::NPQ * C::PANEL;
+          const uint32_t k_addr = sbase + C::OFF_K + kst * C::K_STAGE;
+#pragma unroll
+          for (int ks = 0; ks < C::S_KSTEPS; ++ks) {
+            const uint32_t off =
+                (ks / C::KSTEPS_PER_PANEL) * C::PANEL + (ks % C::KSTEPS_PER_PANEL) * 32;
+            tc_mma_f16(tmem + C::tm_s(t), smem_desc_sw128(q_addr + off, 16, 1024),
+                       smem_desc_sw128(k_addr + off, 16, 1024), C::IDESC_S, ks > 0 ? 1u : 0u);
+          }
+          tc_commit(s_full + 8 * t);
+        };
+        auto issue_pv = [&](int t, int vst, bool first) {
+          const uint32_t v_addr = sbase + C::OFF_V + vst * C::V_STAGE;
+#pragma unroll
+          for (int ks = 0; ks < C::PV_KSTEPS; ++ks)
+            tc_mma_f16_ts(tmem + C::tm_o(t), tmem + C::tm_s(t) + ks * 8,
+                          smem_desc_sw128(v_addr + ks * C::UMMA_K * 128, C::PANEL, 1024),
+                          C::IDESC_PV, (!first || ks > 0) ? 1u : 0u);
+        };
+        // running counts: Q tiles, K and V blocks consumed, p_ready waits and
+        // O tiles per slot
+        int nq = 0, gk = 0, gv = 0;
+        int pc[2] = {0, 0}, od[2] = {0, 0};
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+          const int r = unit_tile(k, n_tiles);
+          if (r < 0) break;
+          PTile T;
+          decode_ptile(p, units, r, qpt, T);
+          if (T.nblk == 0) continue;
+          const int ntiles = T.nq_b > 0 ? 2 : 1;
+          ok = mbar_wait(q_full, nq & 1, p.err, abort_flag) &&
+               mbar_wait(k_full + 8 * (gk % KS), (gk / KS) & 1, p.err, abort_flag);
+          if (!ok) break;
+          ++nq;
+          tc_fence_after();
+          for (int t = 0; t < ntiles; ++t) issue_s(t, gk % KS);
+          tc_commit(k_empty + 8 * (gk % KS));  // K(0) is free once both S(0) are done
+          ++gk;
+          if (T.nblk == 1) tc_commit(q_empty);  // the tile's last S MMAs are issued
+          for (int j = 0; ok && j < T.nblk; ++j) {
+            const int vst = gv % VS;
+            for (int t = 0; t < ntiles; ++t) {
+              ok = mbar_wait(p_ready + 8 * t, pc[t] & 1, p.err, abort_flag);
+              ++pc[t];
+              if (ok && t == 0) ok = mbar_wait(v_full + 8 * vst, (gv / VS) & 1, p.err, abort_flag);
+              if (ok && t == 0 && j + 1 < T.nblk)
+                ok = mbar_wait(k_full + 8 * (gk % KS), (gk / KS) & 1, p.err, abort_flag);
+              // the previous tile's O in this slot has been read out of TMEM
+              if (ok && j == 0 && od[t] > 0)
+                ok = mbar_wait(o_free + 8 * t, (od[t] - 1) & 1, p.err, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(t, vst, j == 0);
+              if (j + 1 < T.nblk) {
+                issue_s(t, gk % KS);
+              } else {
+                tc_commit(o_done + 8 * t);
+                ++od[t];
+              }
+            }
+            if (!ok) break;
+            tc_commit(v_empty + 8 * vst);
+            ++gv;
+            if (j + 1 < T.nblk) {
+              tc_commit(k_empty + 8 * (gk % KS));
+              ++gk;
+            }
+            if (j + 2 == T.nblk) tc_commit(q_empty);  // S(nblk-1) of both tiles issued
+          }
+        }
+        tc_commit(drain);
+        mbar_wait(drain, 0, nullptr, nullptr);
+      }
+    }
+    pdl_launch_dependents();
+    // --------------------------------------------------- teardown (TMA/MMA side)
+    if (warp == 0 && lane == 0 && *abort_flag) {
+      for (int st = 0; st < KS && st < issued_k; ++st) {
+        const int j_last = st + ((issued_k - 1 - st) / KS) * KS;
+        mbar_wait(k_full + 8 * st, (j_last / KS) & 1, nullptr, nullptr);
+      }
+      for (int st = 0; st < VS && st < issued_v; ++st) {
+        const int j_last = st + ((issued_v - 1 - st) / VS) * VS;
+        mbar_wait(v_full + 8 * st, (j_last / VS) & 1, nullptr, nullptr);
+      }
+      if (issued_q > 0) mbar_wait(q_full, (issued_q - 1) & 1, nullptr, nullptr);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+  } else {
+    regs_inc<CP::REGS_SOFTMAX>();
+    // ------------------------------------------------------- softmax warps
+    const int t = (warp - 4) >> 2;  // tile slot 0 (A): warps 4-7, 1 (B): warps 8-11
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const uint32_t s_addr = tmem + lane_base + C::tm_s(t);
+    const uint32_t o_addr = tmem + lane_base + C::tm_o(t);
+    const float sl2 = p.scale * 1.4426950408889634f;
+    int sc = 0, od = 0;  // s_full waits and O tiles of this slot
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int rr = unit_tile(k, n_tiles);
+      if (rr < 0) break;
+      PTile T;
+      decode_ptile(p, units, rr, qpt, T);
+      const int nq = t == 0 ? T.nq_a : T.nq_b;
+      if (nq <= 0) continue;
+      const int nrows = nq * group;
+      const bool warp_active = quarter * 32 < nrows;
+      const bool row_ok = r < nrows;
+      const int i = T.q_start + t * qpt + r / group;
+      const int h = T.kh * group + (r - (r / group) * group);
+      // Rows outside the tile never ask for masking (see fa_umma2.cuh).
+      int lo = -(1 << 30), hi = 1 << 30;
+      if (row_ok) {
+        row_key_range(i, T.sq.lq, T.sq.lk, p.causal, p.window_left, lo, hi);
+        lo = max(lo, T.k0);
+        hi = min(hi, T.k1);
+      }
+      float m_run = -CUDART_INF_F, l_run = 0.f;
+      for (int j = 0; j < T.nblk; ++j) {
+        ok = mbar_wait(s_full + 8 * t, sc & 1, p.err, abort_flag);
+        ++sc;
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+        if (warp_active) {
+          const int kb = T.kb0 + j * kBlockN;
+          float s[128];
+          tmem_ld128(s_addr, reinterpret_cast<uint32_t*>(s));
+          if (__any_sync(0xffffffffu, !(kb >= lo && kb + kBlockN <= hi))) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+              const int key = kb + c;
+              s[c] = (key >= lo && key < hi) ? s[c] : -CUDART_INF_F;
+            }
+          }
+          float mx[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) mx[u] = -CUDART_INF_F;
+#pragma unroll
+          for (int c = 0; c < 128; c += 16)
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mx[u] = fmax3(mx[u], s[c + u], s[c + 8 + u]);
+          const float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+          const float m_new = (bmax > m_run + 8.f) ? bmax : m_run;  // lazy rescale, 2^8
+          const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
+          const float alpha = m_run == m_new ? 1.f : fast_exp2(m_run - m_use);
+          const bool rescale = j > 0 && m_run != -CUDART_INF_F && alpha != 1.f;
+          if (__any_sync(0xffffffffu, rescale)) {
+            // O holds block j-1's result: the S(j) commit covered PV(j-1).
+#pragma unroll
+            for (int c = 0; c < DV / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(o_addr + 32 * c, o);
+#pragma unroll
+              for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+              tmem_st32(o_addr + 32 * c, o);
+            }
+          }
+          const f32x2 sl2x2 = f2_make(sl2, sl2);
+          const f32x2 noff = f2_make(-m_use, -m_use);
+          f32x2 sm[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) sm[u] = 0ull;
+#pragma unroll
+          for (int c = 0; c < 128; c += 2) {
+            const float2 x = f2_split(f2_fma(f2_make(s[c], s[c + 1]), sl2x2, noff));
+            const float e0 = fast_exp2(x.x), e1 = fast_exp2(x.y);
+            s[c] = e0;
+            s[c + 1] = e1;
+            sm[(c >> 1) & 3] = f2_add(sm[(c >> 1) & 3], f2_make(e0, e1));
+          }
+          // P over the first 64 columns of this tile's S buffer (already read)
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) pk[c] = pack2(s[64 * h2 + 2 * c], s[64 * h2 + 2 * c + 1], DT);
+            tmem_st32(s_addr + 32 * h2, pk);
+          }
+          tmem_st_wait();
+          const float2 r01 = f2_split(f2_add(f2_add(sm[0], sm[1]), f2_add(sm[2], sm[3])));
+          l_run = l_run * alpha + (r01.x + r01.y);
+          m_run = m_new;
+        }
+        tc_fence_before();
+        mbar_arrive(p_ready + 8 * t);
+      }
+      if (!ok) break;
+
+      // ------------------------------------------------------------ epilogue
+      if (T.nblk > 0) {
+        ok = mbar_wait(o_done + 8 * t, od & 1, p.err, abort_flag);
+        ++od;
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+      }
+      float inv = 0.f, lse_v = -CUDART_INF_F;
+      if (row_ok && l_run > 0.f && m_run != -CUDART_INF_F) {
+        inv = 1.f / l_run;
+        lse_v = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+      }
+      const int tok = T.sq.q0 + i;
+      uint8_t* orow = static_cast<uint8_t*>(p.out) + ((size_t)tok * p.h_q + h) * (size_t)DV * 2;
+#pragma unroll
+      for (int c = 0; c < DV / 32; ++c) {
+        uint32_t o[32];
+        if (warp_active && T.nblk > 0) {
+          tmem_ld32(o_addr + 32 * c, o);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+        if (warp_active && row_ok) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float* f = reinterpret_cast<const float*>(o) + 8 * e;
+            *reinterpret_cast<uint4*>(orow + c * 64 + e * 16) =
+                make_uint4(pack2(f[0] * inv, f[1] * inv, p.out_dtype),
+                           pack2(f[2] * inv, f[3] * inv, p.out_dtype),
+                           pack2(f[4] * inv, f[5] * inv, p.out_dtype),
+                           pack2(f[6] * inv, f[7] * inv, p.out_dtype));
+          }
+        }
+      }
+      if (T.nblk > 0) {
+        // O has been read out of TMEM: the next tile's first PV may overwrite it
+        tc_fence_before();
+        mbar_arrive(o_free + 8 * t);
+      }
+      if (warp_active && row_ok && p.lse != nullptr) p.lse[(size_t)h * p.total_q + tok] = lse_v;
+    }
+    // teardown (softmax side): the TMEM release waits for these warps
+    tc_fence_before();
+    __syncthreads();
+  }
+}
+
+}  // namespace fa

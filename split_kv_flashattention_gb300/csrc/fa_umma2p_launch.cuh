@@ -1,0 +1,21 @@
+// Launch helper for the persistent two-tile tcgen05 kernel.
+#pragma once
+
+#include "fa_launch.h"
+#include "fa_umma2p.cuh"
+
+namespace fa {
+
+template <int DT, int DQK, int DV, int KS, int VS>
+cudaError_t launch_umma2p_one(const FwdParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                              const CUtensorMap& tmV, dim3 grid, cudaStream_t stream) {
+  using C = Umma2Cfg<DT, DQK, DV, KS, VS>;
+  using CP = Umma2pCfg<DT, DQK, DV, KS, VS>;
+  auto kern = umma2p_splitkv_kernel<DT, DQK, DV, KS, VS>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), CP::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, C::NTHREADS, CP::SMEM, stream>>>(p, tmQ, tmK, tmV);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -387,3 +387,95 @@ def test_running_max_jumps_between_blocks(kernel, growth, causal):
     out, lse = run_gpu(inp, causal=causal, num_splits=1, flags=kernel)
     o_ref, l_ref = reference(inp, 0.0, causal)
     assert_close(inp, out, lse, o_ref, l_ref)
+
+
+# ----------------------------------------- persistent two-tile kernel (AUTO)
+# One split, 16-bit, d <= 128, more than 128 rows per KV head, no mask: AUTO
+# runs the persistent form, which walks a per-CTA tile list (masked cases run
+# the non-persistent kernel and are covered here as well).  Its arithmetic is the
+# two-tile kernel's, so besides the oracle check its output must equal that
+# kernel's bit for bit.
+#
+# Rows that see only one or two keys make O a mix of very few V rows with
+# weights rounded to bf16 for the PV MMA; with O rounded to bf16 too, the
+# error bound is 2^-8 * max|V|, which passes the 1e-2 tolerance only while
+# max|V| < 2.56.  Tests whose subject is the tile walk scale V by 1/4; the
+# bound itself is checked in test_tensor_core_p_rounding_bound.
+
+@pytest.mark.parametrize("mask", ["none", "causal", "window"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_persistent_prefill_edge_lengths(mask, dtype):
+    """The edge-length workload (seed 5, as test_varlen_edge_lengths)."""
+    inp = workload("edge", dtype=dtype, seed=5)
+    causal = mask == "causal"
+    wl = 128 if mask == "window" else -1
+    out, lse = run_gpu(inp, causal=causal, window_left=wl, num_splits=1, guard_rows=2)
+    o_ref, l_ref = reference(inp, 0.0, causal, wl)
+    assert_close(inp, out, lse, o_ref, l_ref)
+    out2, lse2 = run_gpu(inp, causal=causal, window_left=wl, num_splits=1, guard_rows=2,
+                         flags=fa.FA_KERNEL_UMMA2)
+    assert np.array_equal(out, out2, equal_nan=True) and np.array_equal(lse, lse2, equal_nan=True)
+
+
+@pytest.mark.parametrize("mask", ["causal", "window"])
+def test_tensor_core_p_rounding_bound(mask):
+    """Edge lengths on another seed, where a causal row with two keys and
+    |V| near 4.5 puts the bf16 rounding of P and O at about 1.07e-2: the
+    error stays within 2^-8 * max|V| (P weights and O each rounded to bf16,
+    relative 2^-9), and LSE, which uses the fp32 row sums, within 1e-3."""
+    inp = workload("edge", dtype="bf16", seed=41)
+    causal = mask == "causal"
+    wl = 128 if mask == "window" else -1
+    out, lse = run_gpu(inp, causal=causal, window_left=wl, num_splits=1)
+    o_ref, l_ref = reference(inp, 0.0, causal, wl)
+    tq = inp.q.shape[0]
+    bound = 2.0 ** -8 * float(inp.v.float().abs().max()) + 1e-4
+    assert np.abs(out[:tq] - o_ref).max() <= bound
+    fin = np.isfinite(l_ref)
+    assert np.array_equal(np.isneginf(lse[:, :tq]), np.isneginf(l_ref))
+    assert np.abs(lse[:, :tq][fin] - l_ref[fin]).max() <= 1e-3
+
+
+def _quarter_v(inp):
+    inp.v = (inp.v.float() * 0.25).to(inp.v.dtype)
+    return inp
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_persistent_prefill_many_tiles(causal):
+    """More (sequence, head, query pair) tiles than SMs, skewed lengths, d=64,
+    GQA 8:1: every CTA walks several tiles of different sizes."""
+    lens = [1500, 257, 0, 900, 64, 1, 700, 2048, 300, 513]
+    inp = _quarter_v(make_inputs(lens, lens, 16, 2, 64, 64, "bf16", seed=42))
+    out, lse = run_gpu(inp, causal=causal, num_splits=1)
+    o_ref, l_ref = reference(inp, 0.0, causal)
+    assert_close(inp, out, lse, o_ref, l_ref)
+    out2, lse2 = run_gpu(inp, causal=causal, num_splits=1, flags=fa.FA_KERNEL_UMMA2)
+    assert np.array_equal(out, out2, equal_nan=True) and np.array_equal(lse, lse2, equal_nan=True)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_persistent_prefill_q_and_k_lengths_differ(causal):
+    """Lq != Lk (bottom-right causal: early query rows may see no key, so some
+    tiles have no key block at all) and a sequence with queries but no keys."""
+    lens_q, lens_k = [300, 129, 600, 40, 200], [100, 900, 600, 0, 450]
+    inp = _quarter_v(make_inputs(lens_q, lens_k, 8, 4, 128, 128, "bf16", seed=43))
+    out, lse = run_gpu(inp, causal=causal, num_splits=1)
+    o_ref, l_ref = reference(inp, 0.0, causal)
+    assert_close(inp, out, lse, o_ref, l_ref)
+
+
+def test_persistent_prefill_running_max_jumps():
+    lens = [700, 300, 520]
+    inp = _quarter_v(make_inputs(lens, lens, 2, 2, 128, 128, "bf16", seed=44))
+    k = inp.k.float()
+    cu = inp.cu_seqlens_k.tolist()
+    for b in range(len(lens)):
+        for blk, f in enumerate([1.0, 1.0, 8.0, 8.0, 40.0, 1.0]):
+            r0, r1 = cu[b] + 128 * blk, min(cu[b + 1], cu[b] + 128 * blk + 128)
+            if r0 < r1:
+                k[r0:r1] *= f
+    inp.k = k.to(inp.k.dtype)
+    out, lse = run_gpu(inp, causal=True, num_splits=1)
+    o_ref, l_ref = reference(inp, 0.0, True)
+    assert_close(inp, out, lse, o_ref, l_ref)

@@ -107,15 +107,18 @@ typedef enum {
  *                 "Implementation": the default scale uses the head dim).
  *  causal, window_left  masks, see above.
  *  num_splits     0 = automatic (fa_plan), else 1..128 splits of the key range.
- *  out            device [total_q, h_q, d_v] of out_dtype (bf16 or fp16);
- *                 rows of sequences are written, other rows are untouched.
+ *  out            device [total_q, h_q, d_v] of out_dtype; rows of sequences
+ *                 are written, other rows are untouched.
  *  lse            device float32 [h_q, total_q] or NULL.
  *  workspace      device scratch of >= fa_fwd_splitkv_workspace_size(...)
  *                 bytes when the resolved split count is > 1 (else may be NULL);
  *                 contents need no initialisation and are clobbered.
  *  workspace_bytes size of workspace (checked).
- *  in_dtype, out_dtype  FA_BF16 / FA_FP16 / FA_E4M3 inputs; out is bf16 or
- *                 fp16 (equal to in_dtype for 16-bit inputs).
+ *  in_dtype, out_dtype  FA_BF16 / FA_FP16 / FA_E4M3 inputs.  Out is in_dtype
+ *                 or FA_E4M3 for 16-bit inputs, and any of the three for e4m3
+ *                 inputs.  An e4m3 O is the value itself rounded to nearest
+ *                 even and saturated to +-448, with no output scale (the
+ *                 pages define no fp8 output; this is the plainest form).
  *  descale_q/k/v  device float32 scalars, required for FA_E4M3 inputs
  *                 (per-tensor dequantisation factors), ignored otherwise.
  *  flags          FA_KERNEL_* selection, optionally OR FA_RUN_*_ONLY.  AUTO
@@ -123,7 +126,10 @@ typedef enum {
  *                 group) per KV head (2 for e4m3 with d_qk=192), the
  *                 one-tile tcgen05 kernel up to 128 rows, for e4m3 and for
  *                 head dim 256, and the two-tile tcgen05 kernel beyond 128
- *                 rows (16-bit, head dim <= 128).
+ *                 rows (16-bit, head dim <= 128; its persistent form for one
+ *                 split over packed K/V without a mask, at most 128
+ *                 sequences).  FA_KERNEL_UMMA2 always runs the non-persistent
+ *                 two-tile kernel.
  *  stream         cudaStream_t.
  * Returns FA_OK or a negative fa_status.
  */

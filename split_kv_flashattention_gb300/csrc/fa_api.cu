@@ -319,8 +319,9 @@ int fwd_impl(const void* q, const void* k, const void* v, const int* cu_seqlens_
   if (h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || h_q / h_kv > 128) return FA_ERR_INVALID_ARG;
   if (num_splits < 0 || num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
   if (in_dtype != kBF16 && in_dtype != kFP16 && in_dtype != kE4M3) return FA_ERR_INVALID_ARG;
-  if (out_dtype != kBF16 && out_dtype != kFP16) return FA_ERR_INVALID_ARG;
-  if (in_dtype != kE4M3 && out_dtype != in_dtype) return FA_ERR_UNSUPPORTED;
+  if (out_dtype != kBF16 && out_dtype != kFP16 && out_dtype != kE4M3) return FA_ERR_INVALID_ARG;
+  // 16-bit inputs write their own type or e4m3; e4m3 inputs write any of the three
+  if (in_dtype != kE4M3 && out_dtype != in_dtype && out_dtype != kE4M3) return FA_ERR_UNSUPPORTED;
   if (!dims_supported(in_dtype, d_qk, d_v)) return FA_ERR_UNSUPPORTED;
   if (isnan(scale) || isinf(scale)) return FA_ERR_INVALID_ARG;
   const int kernel_sel = flags & FA_KERNEL_MASK;

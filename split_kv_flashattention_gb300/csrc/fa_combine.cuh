@@ -125,17 +125,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ Fw
     }
   }
 
-  uint8_t* orow = static_cast<uint8_t*>(p.out) + ((size_t)t * p.h_q + h) * (size_t)DV * 2;
-  uint32_t pk[DPL / 2];
-#pragma unroll
-  for (int e = 0; e < DPL / 2; ++e) pk[e] = pack2(acc[2 * e], acc[2 * e + 1], p.out_dtype);
-  if constexpr (DPL == 8) {
-    *reinterpret_cast<uint4*>(orow + lane * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-  } else if constexpr (DPL == 4) {
-    *reinterpret_cast<uint2*>(orow + lane * 8) = make_uint2(pk[0], pk[1]);
-  } else {
-    *reinterpret_cast<uint32_t*>(orow + lane * 4) = pk[0];
-  }
+  store_o<DPL>(p.out, ((size_t)t * p.h_q + h) * DV + lane * DPL, acc, 1.f, p.out_dtype);
   if (p.lse != nullptr && lane == 0) p.lse[(size_t)h * p.total_q + t] = lse_out;
 }
 

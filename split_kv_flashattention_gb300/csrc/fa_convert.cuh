@@ -131,4 +131,51 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, int out_dtype) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// N consecutive output elements (already normalised, times `scale`) at
+// element index `elem` of O: 16-bit types as 2N bytes (round to nearest), e4m3
+// as N bytes (round to nearest even, saturating to +-448).  N is 2, 4, 8 or
+// 32; the address is aligned to the store width (2N or N bytes).
+template <int N>
+__device__ __forceinline__ void store_o(void* out, size_t elem, const float* f, float scale,
+                                        int out_dtype) {
+  static_assert(N == 2 || N == 4 || N == 8 || N == 32, "store width");
+  if (out_dtype == kE4M3) {
+    uint8_t* dst = static_cast<uint8_t*>(out) + elem;
+    uint32_t w[(N + 3) / 4];
+#pragma unroll
+    for (int i = 0; i < (N + 3) / 4; ++i) w[i] = 0u;
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+      const uint32_t two = (uint32_t)__nv_cvt_float2_to_fp8x2(
+          make_float2(f[i] * scale, f[i + 1] * scale), __NV_SATFINITE, __NV_E4M3);
+      w[i / 4] |= two << (8 * (i % 4));
+    }
+    if constexpr (N == 2) {
+      *reinterpret_cast<uint16_t*>(dst) = (uint16_t)w[0];
+    } else if constexpr (N == 4) {
+      *reinterpret_cast<uint32_t*>(dst) = w[0];
+    } else if constexpr (N == 8) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < N / 16; ++i)
+        reinterpret_cast<uint4*>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    }
+  } else {
+    uint8_t* dst = static_cast<uint8_t*>(out) + elem * 2;
+    uint32_t w[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) w[i] = pack2(f[2 * i] * scale, f[2 * i + 1] * scale, out_dtype);
+    if constexpr (N == 2) {
+      *reinterpret_cast<uint32_t*>(dst) = w[0];
+    } else if constexpr (N == 4) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < N / 8; ++i)
+        reinterpret_cast<uint4*>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    }
+  }
+}
+
 }  // namespace fa

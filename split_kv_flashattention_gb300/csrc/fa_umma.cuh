@@ -525,14 +525,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(o[e]) * inv;
         if (p.num_splits == 1) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) +
-                                                ((size_t)t * p.h_q + h) * (size_t)DV * 2 + c * 64);
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[e] = make_uint4(pack2(f[8 * e], f[8 * e + 1], p.out_dtype),
-                                pack2(f[8 * e + 2], f[8 * e + 3], p.out_dtype),
-                                pack2(f[8 * e + 4], f[8 * e + 5], p.out_dtype),
-                                pack2(f[8 * e + 6], f[8 * e + 7], p.out_dtype));
+          store_o<32>(p.out, ((size_t)t * p.h_q + h) * DV + c * 32, f, 1.f, p.out_dtype);
         } else {
           const size_t slot = (size_t)b * p.max_seqlen_q + i;
           float4* dst = reinterpret_cast<float4*>(

@@ -544,7 +544,6 @@ __global__ void __launch_bounds__(384, 1)
         lse_v = (m_run + __log2f(l_run)) * 0.69314718055994531f;
       }
       const int tok = T.sq.q0 + i;
-      uint8_t* orow = static_cast<uint8_t*>(p.out) + ((size_t)tok * p.h_q + h) * (size_t)DV * 2;
 #pragma unroll
       for (int c = 0; c < DV / 32; ++c) {
         uint32_t o[32];
@@ -554,17 +553,9 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = 0u;
         }
-        if (warp_active && row_ok) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float* f = reinterpret_cast<const float*>(o) + 8 * e;
-            *reinterpret_cast<uint4*>(orow + c * 64 + e * 16) =
-                make_uint4(pack2(f[0] * inv, f[1] * inv, p.out_dtype),
-                           pack2(f[2] * inv, f[3] * inv, p.out_dtype),
-                           pack2(f[4] * inv, f[5] * inv, p.out_dtype),
-                           pack2(f[6] * inv, f[7] * inv, p.out_dtype));
-          }
-        }
+        if (warp_active && row_ok)
+          store_o<32>(p.out, ((size_t)tok * p.h_q + h) * DV + c * 32,
+                      reinterpret_cast<const float*>(o), inv, p.out_dtype);
       }
       if (T.nblk > 0) {
         // O has been read out of TMEM: the next tile's first PV may overwrite it

@@ -107,7 +107,8 @@ def _call_ex(fa, **kw):
     (dict(d_qk=192, d_v=128), -2),                 # 192 only for e4m3
     (dict(in_dtype=0, out_dtype=1), -2),           # bf16 in, fp16 out
     (dict(in_dtype=7), -1),
-    (dict(out_dtype=2), -1),                       # fp8 output
+    (dict(out_dtype=3), -1),                       # unknown output type
+    (dict(in_dtype=1, out_dtype=0), -2),           # fp16 in, bf16 out
     (dict(q=0x1008), -1),                          # unaligned q
     (dict(out=0x6004), -1),                        # unaligned out
     (dict(lse=0x7002), -1),                        # unaligned lse

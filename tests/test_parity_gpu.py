@@ -479,3 +479,75 @@ def test_persistent_prefill_running_max_jumps():
     out, lse = run_gpu(inp, causal=True, num_splits=1)
     o_ref, l_ref = reference(inp, 0.0, True)
     assert_close(inp, out, lse, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("kernel", [fa.FA_KERNEL_AUTO] + KERNELS)
+@pytest.mark.parametrize("h_kv", [8, 2, 1])
+@pytest.mark.parametrize("mask", ["none", "causal", "window"])
+def test_edge_lengths_gqa_matrix(kernel, h_kv, mask):
+    """cutlass varlen page, "Tests": the edge lengths (1, 0, 63, 64, 65, 128,
+    129, 700) x GQA 8:8, 8:2, 8:1 x no mask / causal / window (128, 0), on
+    every kernel (AUTO runs the persistent kernel without a mask). V / 2
+    keeps the bf16 rounding bound 2^-8 max|V| of rows with one or two keys
+    under the 1e-2 tolerance (see test_tensor_core_p_rounding_bound)."""
+    lens = [1, 0, 63, 64, 65, 128, 129, 700]
+    inp = make_inputs(lens, lens, 8, h_kv, 128, 128, "bf16", seed=45)
+    inp.v = (inp.v.float() * 0.5).to(inp.v.dtype)
+    causal = mask == "causal"
+    wl = 128 if mask == "window" else -1
+    out, lse = run_gpu(inp, causal=causal, window_left=wl, num_splits=1, flags=kernel)
+    o_ref, l_ref = reference(inp, 0.0, causal, wl)
+    assert_close(inp, out, lse, o_ref, l_ref)
+
+
+# ------------------------------------------------------------- fp8 output
+# e4m3 O: the value rounded to nearest even and saturated to +-448; the
+# rounding adds at most half an e4m3 ulp, 2^-4 of |O|, to the input type's
+# tolerance.
+
+def _assert_close_e4m3_out(inp, out, lse, o_ref, l_ref):
+    atol = {"bf16": 1e-2, "fp16": 1e-2, "e4m3": 0.13}[inp.dtype]
+    tq = inp.q.shape[0]
+    ref = np.clip(o_ref, -448.0, 448.0)
+    assert np.isfinite(out[:tq]).all()
+    err = np.abs(out[:tq] - ref) - (atol + 2.0 ** -4 * np.abs(ref))
+    assert err.max() <= 0, f"max|dO|={np.abs(out[:tq] - ref).max():.4g}"
+    fin = np.isfinite(l_ref)
+    assert np.array_equal(np.isneginf(lse[:, :tq]), np.isneginf(l_ref))
+    assert np.abs(lse[:, :tq][fin] - l_ref[fin]).max() <= 1e-3
+
+
+@pytest.mark.parametrize("kernel,lens_q,ns", [
+    (fa.FA_KERNEL_SIMT, [1, 1, 1], 3),             # decode rows, split + combine
+    (fa.FA_KERNEL_SIMT, [1, 1, 1], 1),
+    (fa.FA_KERNEL_UMMA, [40, 3, 70], 1),
+    (fa.FA_KERNEL_UMMA, [40, 3, 70], 4),
+    (fa.FA_KERNEL_UMMA2, [300, 129, 5], 1),
+    (fa.FA_KERNEL_AUTO, [300, 129, 5], 1),          # persistent kernel
+])
+@pytest.mark.parametrize("in_dtype", ["bf16", "e4m3"])
+def test_fp8_output(kernel, lens_q, ns, in_dtype):
+    if in_dtype == "e4m3" and kernel in (fa.FA_KERNEL_UMMA2, fa.FA_KERNEL_AUTO) and max(lens_q) > 128:
+        kernel = fa.FA_KERNEL_UMMA  # the two-tile kernels take 16-bit inputs
+    lens_k = [700, 260, 1300]
+    inp = make_inputs(lens_q, lens_k, 4, 2, 128, 128, in_dtype, seed=46)
+    out, lse = run_gpu(inp, num_splits=ns, flags=kernel, out_dtype=torch.float8_e4m3fn)
+    o_ref, l_ref = reference(inp)
+    _assert_close_e4m3_out(inp, out, lse, o_ref, l_ref)
+
+
+def test_fp8_output_saturates():
+    """|O| far beyond the e4m3 range: written as +-448, not inf or NaN."""
+    inp = make_inputs([1, 200], [300, 500], 2, 2, 128, 128, "bf16", seed=47)
+    # O is a convex mix of V rows: a large per-column constant (+-600) puts
+    # every O element beyond the e4m3 range whatever the weights are.
+    col_sign = torch.where(torch.arange(inp.d_v) % 2 == 0, 1.0, -1.0)
+    inp.v = (600.0 * col_sign + 0.1 * inp.v.float()).to(inp.v.dtype)
+    for kernel in (fa.FA_KERNEL_SIMT, fa.FA_KERNEL_UMMA, fa.FA_KERNEL_AUTO):
+        out, lse = run_gpu(inp, num_splits=1, flags=kernel, out_dtype=torch.float8_e4m3fn)
+        o_ref, l_ref = reference(inp)
+        tq = inp.q.shape[0]
+        assert np.isfinite(out[:tq]).all() and np.abs(out[:tq]).max() <= 448.0
+        big = np.abs(o_ref) > 480.0
+        assert big.any() and np.array_equal(np.sign(out[:tq][big]), np.sign(o_ref[big]))
+        assert np.all(np.abs(out[:tq][big]) == 448.0)

@@ -77,4 +77,25 @@ cudaError_t launch_split_ranges(const int* cu_q, const int* cu_k, int batch, int
 // device; thread-safe).
 cudaError_t ensure_smem_attr(const void* kernel, int bytes);
 
+// Launches a partial kernel with programmatic stream serialisation: its CTAs
+// may be scheduled while the previous kernel in the stream drains, and the
+// kernel waits for that kernel (griddepcontrol.wait) before its first global
+// memory access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, int threads, int smem,
+                             cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 }  // namespace fa

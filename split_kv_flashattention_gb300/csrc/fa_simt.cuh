@@ -96,6 +96,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
+  pdl_wait();  // the previous kernel in the stream is complete from here on
   int* rank_scratch = reinterpret_cast<int*>(smem + C::OFF_RANK);
   // The order is a compile-time choice: the kernel's decode loop is sensitive
   // to the code around it, and the grid-order variant keeps single-sequence

@@ -36,8 +36,7 @@ cudaError_t launch_simt_one(const FwdParams& p, const CUtensorMap& tmK, const CU
   auto kern = simt_splitkv_kernel<DT, DQK, DV, RT, NW, NS, ORDERED>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, C::NTHREADS, C::SMEM, stream>>>(p, tmK, tmV);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, C::NTHREADS, C::SMEM, stream, p, tmK, tmV);
 }
 
 template <int DT, int DQK, int DV, int RTMAX, bool ORDERED>

@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(192, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
+  pdl_wait();  // the previous kernel in the stream is complete from here on
   // The sequence offsets are loaded before the error-word check so that both
   // reads share one memory latency.
   SeqInfo sq;

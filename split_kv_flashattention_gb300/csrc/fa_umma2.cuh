@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(384, 1)
   const int group = p.group;
   const int qpt = 128 / group;
 
+  pdl_wait();  // the previous kernel in the stream is complete from here on
   if (__syncthreads_or(timed_out_before(p.err))) return;
   SeqInfo sq;
   if (!load_seq(p, b, sq)) {

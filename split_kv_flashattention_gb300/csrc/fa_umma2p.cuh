@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(384, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
+  pdl_wait();  // the previous kernel in the stream is complete from here on
   if (__syncthreads_or(timed_out_before(p.err))) return;
 
   // ---- the tile list: units (sequence, query pair) that exist, longest first

@@ -14,8 +14,7 @@ cudaError_t launch_umma2p_one(const FwdParams& p, const CUtensorMap& tmQ, const 
   auto kern = umma2p_splitkv_kernel<DT, DQK, DV, KS, VS>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), CP::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, C::NTHREADS, CP::SMEM, stream>>>(p, tmQ, tmK, tmV);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, C::NTHREADS, CP::SMEM, stream, p, tmQ, tmK, tmV);
 }
 
 }  // namespace fa

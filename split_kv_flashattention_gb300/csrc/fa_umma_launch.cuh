@@ -14,8 +14,7 @@ cudaError_t launch_umma_one(const FwdParams& p, const CUtensorMap& tmQ, const CU
   auto kern = umma_splitkv_kernel<DT, DQK, DV, KS, VS>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, C::NTHREADS, C::SMEM, stream>>>(p, tmQ, tmK, tmV);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, C::NTHREADS, C::SMEM, stream, p, tmQ, tmK, tmV);
 }
 
 }  // namespace fa

@@ -398,6 +398,10 @@ int fwd_impl(const void* q, const void* k, const void* v, const int* cu_seqlens_
   p.page_size = paged ? page_size : 0;
   p.page_shift = 0;
   while (paged && (1 << p.page_shift) < page_size) ++p.page_shift;
+  // SM count (already queried for an automatic split count; a failed query
+  // only disables the kernels' look-ahead prefetch)
+  p.num_sms = sms;
+  if (num_splits != 0 && device_sms(&p.num_sms) != FA_OK) p.num_sms = 0;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 

@@ -56,6 +56,7 @@ struct FwdParams {
   int max_pages;
   int page_size;    // 0: contiguous packed K/V addressed through cu_k
   int page_shift;   // log2(page_size)
+  int num_sms;      // SMs of the device (0 if unknown)
 };
 
 struct SeqInfo {
@@ -168,9 +169,8 @@ __device__ __forceinline__ TileIdx grid_order_tile(const FwdParams& p) {
 // causal or window mask a tile's work grows with its index m and hardly
 // depends on the sequence, so the tiles run m-major (all sequences' last
 // tiles first): a longest-first order computed from the block index alone.
-__device__ __forceinline__ TileIdx query_tile_order(const FwdParams& p) {
+__device__ __forceinline__ TileIdx query_tile_order_at(const FwdParams& p, int x, int y, int z) {
   TileIdx t;
-  int x = blockIdx.x, y = blockIdx.y;
   if (p.causal || p.window_left >= 0) {
     const int lin = x + gridDim.x * y;
     x = lin / gridDim.y;
@@ -179,8 +179,12 @@ __device__ __forceinline__ TileIdx query_tile_order(const FwdParams& p) {
   t.m_blk = gridDim.x - 1 - x;
   t.b = y / p.h_kv;
   t.kh = y - t.b * p.h_kv;
-  t.split = blockIdx.z;
+  t.split = z;
   return t;
+}
+
+__device__ __forceinline__ TileIdx query_tile_order(const FwdParams& p) {
+  return query_tile_order_at(p, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
 // Every thread of the CTA calls this: it holds two barriers.  `keys` and

@@ -229,6 +229,39 @@ __global__ void __launch_bounds__(384, 1)
           issued_v = jv + 1;
         }
       }
+      // The CTA this SM most likely runs next (CTAs are dispatched in linear
+      // block order, one per SM): its Q and first K/V block into L2, so its
+      // prologue does not wait on DRAM for them.
+      if (p.num_sms > 0 && p.page_size <= 0) {
+        const long long lin =
+            blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
+        const long long nxt = lin + p.num_sms;
+        if (nxt < (long long)gridDim.x * gridDim.y * gridDim.z) {
+          const int x2 = (int)(nxt % gridDim.x);
+          const long long r2 = nxt / gridDim.x;
+          const TileIdx t2 = query_tile_order_at(p, x2, (int)(r2 % gridDim.y), (int)(r2 / gridDim.y));
+          SeqInfo s2;
+          const int qs2 = t2.m_blk * 2 * qpt;
+          if (load_seq(p, t2.b, s2) && qs2 < s2.lq) {
+            const int nq2 = min(2 * qpt, s2.lq - qs2);
+            for (int t = 0; t * qpt < nq2; ++t)
+#pragma unroll
+              for (int pq = 0; pq < C::NPQ; ++pq)
+                tma_prefetch_l2_3d(&tmQ, pq * C::PANEL_ELEMS, t2.kh * group, s2.q0 + qs2 + t * qpt);
+            int a0, a1;
+            tile_split_range(qs2, qs2 + nq2 - 1, s2.lq, s2.lk, p.causal, p.window_left,
+                             p.num_splits, t2.split, a0, a1);
+            if (a1 > a0) {
+#pragma unroll
+              for (int pk = 0; pk < C::NPQ; ++pk)
+                tma_prefetch_l2_3d(&tmK, pk * C::PANEL_ELEMS, t2.kh, s2.k0 + a0);
+#pragma unroll
+              for (int pv = 0; pv < C::NPV; ++pv)
+                tma_prefetch_l2_3d(&tmV, pv * C::PANEL_ELEMS, t2.kh, s2.k0 + a0);
+            }
+          }
+        }
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA

@@ -236,6 +236,15 @@ FA_API int fa_debug_split_ranges(const int* cu_seqlens_q, const int* cu_seqlens_
                           int max_seqlen_q, int causal, int window_left, int num_splits,
                           int tile_queries, int* ranges_out, void* stream);
 
+/* Test hook (no counterpart in the pages): enqueues one CTA whose single
+ * thread waits, with the kernels' own bounded mbarrier wait, on a phase that
+ * nothing completes.  After timeout_ms (1..10000) the wait gives up, records
+ * FA_ERR_DEVICE_TIMEOUT in the device error word (if no error is recorded
+ * yet) and the kernel returns; the context stays usable.  While the word
+ * holds FA_ERR_DEVICE_TIMEOUT, the forward kernels skip their work.
+ * Returns FA_ERR_INVALID_ARG for a timeout outside 1..10000 ms. */
+FA_API int fa_debug_wait_timeout(unsigned int timeout_ms, void* stream);
+
 /* Sticky device error word of the current device (FA_OK if none).  Waits
  * for the device to finish its work.  clear != 0 resets the word. */
 FA_API int fa_get_device_error(int clear);

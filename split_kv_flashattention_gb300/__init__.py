@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "FaError", "FaLibraryMissing", "library", "fa_fwd_splitkv_ex", "fa_fwd_splitkv",
-    "fa_fwd_splitkv_workspace_size", "fa_plan", "fa_debug_split_ranges",
+    "fa_fwd_splitkv_workspace_size", "fa_plan", "fa_debug_split_ranges", "fa_debug_wait_timeout",
     "fa_get_device_error", "fa_status_string", "fa_version", "forward",
     "FA_KERNEL_AUTO", "FA_KERNEL_SIMT", "FA_KERNEL_UMMA", "FA_KERNEL_UMMA2", "FA_RUN_PARTIAL_ONLY",
     "FA_RUN_COMBINE_ONLY", "DTYPE_CODES", "fa_fwd_splitkv_noalloc", "NOALLOC_SCRATCH_BYTES",
@@ -34,7 +34,7 @@ DTYPE_CODES = {torch.bfloat16: 0, torch.float16: 1, torch.float8_e4m3fn: 2}
 EXPORTED = (
     "fa_fwd_splitkv_ex", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_plan",
     "fa_debug_split_ranges", "fa_get_device_error", "fa_status_string", "fa_version",
-    "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_paged",
+    "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_paged", "fa_debug_wait_timeout",
 )
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -87,6 +87,8 @@ def library() -> ctypes.CDLL:
     lib.fa_plan.argtypes = [_c_int] * 6 + [ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]
     lib.fa_debug_split_ranges.restype = _c_int
     lib.fa_debug_split_ranges.argtypes = [_vp, _vp] + [_c_int] * 6 + [_vp, _vp]
+    lib.fa_debug_wait_timeout.restype = _c_int
+    lib.fa_debug_wait_timeout.argtypes = [ctypes.c_uint, _vp]
     lib.fa_get_device_error.restype = _c_int
     lib.fa_get_device_error.argtypes = [_c_int]
     lib.fa_status_string.restype = ctypes.c_char_p
@@ -133,6 +135,12 @@ def fa_fwd_splitkv_workspace_size(batch: int, max_seqlen_q: int, h_q: int, h_kv:
                                   num_splits: int = 0) -> int:
     return int(library().fa_fwd_splitkv_workspace_size(batch, max_seqlen_q, h_q, h_kv, d_v,
                                                        num_splits))
+
+
+def fa_debug_wait_timeout(timeout_ms: int, stream=None):
+    """Test hook: a bounded device wait that runs out after timeout_ms and
+    records FA_ERR_DEVICE_TIMEOUT (see the C header)."""
+    _check(library().fa_debug_wait_timeout(int(timeout_ms), _stream(stream)), "fa_debug_wait_timeout")
 
 
 def fa_get_device_error(clear: bool = False) -> int:

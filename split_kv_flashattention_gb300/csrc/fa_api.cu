@@ -285,6 +285,16 @@ int fa_get_device_error(int clear) {
   return v;
 }
 
+int fa_debug_wait_timeout(unsigned int timeout_ms, void* stream) {
+  if (timeout_ms < 1 || timeout_ms > 10000) return FA_ERR_INVALID_ARG;
+  int* err = nullptr;
+  const int st = device_error_ptr(&err);
+  if (st != FA_OK) return st;
+  wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      err, (unsigned long long)timeout_ms * 1000000ull);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 int fa_debug_split_ranges(const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
                           int max_seqlen_q, int causal, int window_left, int num_splits,
                           int tile_queries, int* ranges_out, void* stream) {

@@ -36,6 +36,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ Fw
   const bool valid = in_grid && load_seq(p, b, sq) && i < sq.lq;  // bad offsets: reported by the partial kernel
   pdl_wait();
   if (!valid) return;
+  // A recorded timeout means the partials are incomplete: write nothing (the
+  // word is read with the partials, in the same round of loads).
+  const bool timed_out = timed_out_before(p.err);
   const int t = sq.q0 + i;
   const int ns = p.num_splits;
   const size_t split_stride = (size_t)p.slots * p.h_q;
@@ -125,8 +128,25 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ Fw
     }
   }
 
+  if (timed_out) return;
   store_o<DPL>(p.out, ((size_t)t * p.h_q + h) * DV + lane * DPL, acc, 1.f, p.out_dtype);
   if (p.lse != nullptr && lane == 0) p.lse[(size_t)h * p.total_q + t] = lse_out;
+}
+
+// Test hook: one thread waits, through the kernels' own bounded wait, on an
+// mbarrier phase that no thread ever completes.  The wait gives up after
+// timeout_ns, records FA_ERR_DEVICE_TIMEOUT in the device error word and the
+// kernel returns: the path a broken pipeline takes, without breaking one.
+__global__ void wait_timeout_kernel(int* err, unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, err, &abort_flag, timeout_ns);
 }
 
 // Test hook: the per-split key ranges the kernels compute, for a tile of

@@ -78,7 +78,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // already recorded a timeout (so a broken pipeline costs one timeout, not
 // one per CTA).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err,
-                                          volatile int* abort) {
+                                          volatile int* abort,
+                                          unsigned long long timeout_ns = FA_WAIT_TIMEOUT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -89,7 +90,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* er
         if (abort) *abort = 1;
         return false;
       }
-      if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) {
+      if (globaltimer_ns() - t0 > timeout_ns) {
         record_error(err, kErrDeviceTimeout);
         if (abort) *abort = 1;
         return false;

@@ -163,3 +163,9 @@ def test_paged_argument_errors(fa, kw, status):
 
 def test_paged_empty_problem_is_a_noop(fa):
     assert _call_paged(fa, batch=0) == 0
+
+
+@pytest.mark.parametrize("timeout_ms", [0, 10001])
+def test_wait_timeout_hook_rejects_bad_timeouts(fa, timeout_ms):
+    """The bounded-wait test hook validates its timeout before any CUDA call."""
+    assert fa.library().fa_debug_wait_timeout(timeout_ms, None) == -1

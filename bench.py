@@ -447,10 +447,10 @@ def main():
         if rows <= simt_rows:
             kern_tag = "simt_splitkv"
         elif rows > 128 and inp.dtype != "e4m3" and inp.d_qk <= 128:
-            # the persistent form: one split, packed K/V, no mask, tile list fits
+            # the persistent form: one split, packed K/V, a workspace, tile list fits
             qpt = 128 // (inp.h_q // inp.h_kv)
             pairs = -(-inp.max_seqlen_q // (2 * qpt))
-            persistent = (ns == 1 and not paged and not causal and inp.batch <= 128
+            persistent = (ns == 1 and not paged and ws is not None and inp.batch <= 128
                           and pairs <= 512 and inp.batch * pairs <= 640)
             kern_tag = "umma2p_splitkv" if persistent else "umma2_splitkv"
         else:

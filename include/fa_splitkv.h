@@ -111,8 +111,11 @@ typedef enum {
  *                 are written, other rows are untouched.
  *  lse            device float32 [h_q, total_q] or NULL.
  *  workspace      device scratch of >= fa_fwd_splitkv_workspace_size(...)
- *                 bytes when the resolved split count is > 1 (else may be NULL);
- *                 contents need no initialisation and are clobbered.
+ *                 bytes, 16-byte aligned.  Required when the resolved split
+ *                 count is > 1.  With one split it may be NULL: it then only
+ *                 holds the persistent kernel's 16-byte tile counter, and
+ *                 without it the non-persistent grid runs instead.  Contents
+ *                 need no initialisation and are clobbered (in stream order).
  *  workspace_bytes size of workspace (checked).
  *  in_dtype, out_dtype  FA_BF16 / FA_FP16 / FA_E4M3 inputs.  Out is in_dtype
  *                 or FA_E4M3 for 16-bit inputs, and any of the three for e4m3
@@ -127,7 +130,7 @@ typedef enum {
  *                 one-tile tcgen05 kernel up to 128 rows, for e4m3 and for
  *                 head dim 256, and the two-tile tcgen05 kernel beyond 128
  *                 rows (16-bit, head dim <= 128; its persistent form for one
- *                 split over packed K/V without a mask, at most 128
+ *                 split over packed K/V with a workspace, at most 128
  *                 sequences).  FA_KERNEL_UMMA2 always runs the non-persistent
  *                 two-tile kernel.
  *  stream         cudaStream_t.
@@ -207,9 +210,9 @@ FA_API int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v,
 
 /* Bytes of workspace fa_fwd_splitkv_ex needs for these sizes: the fp32
  * partial outputs [ns, batch*max_seqlen_q, h_q, d_v] followed by the partial
- * LSEs [ns, batch*max_seqlen_q, h_q]; 0 when the resolved split count is 1.
- * num_splits = 0 resolves the automatic count on the current device. Returns
- * 0 for invalid sizes as well. */
+ * LSEs [ns, batch*max_seqlen_q, h_q]; 16 (the persistent kernel's tile
+ * counter) when the resolved split count is 1.  num_splits = 0 resolves the
+ * automatic count on the current device.  Returns 0 for invalid sizes. */
 FA_API size_t fa_fwd_splitkv_workspace_size(int batch, int max_seqlen_q, int h_q, int h_kv, int d_v,
                                      int num_splits);
 

@@ -267,7 +267,7 @@ size_t fa_fwd_splitkv_workspace_size(int batch, int max_seqlen_q, int h_q, int h
     if (device_sms(&sms) != FA_OK) return 0;
     plan_impl(batch, max_seqlen_q, h_q, h_kv, 0, sms, &ns, nullptr);
   }
-  if (ns <= 1) return 0;
+  if (ns <= 1) return kSchedBytes;  // the persistent kernel's ticket counter
   const size_t slots = (size_t)batch * max_seqlen_q * h_q;
   return 4 * (size_t)ns * slots * (size_t)(d_v + 1);
 }
@@ -442,15 +442,16 @@ int fwd_impl(const void* q, const void* k, const void* v, const int* cu_seqlens_
       CUtensorMap tmQ;
       st = make_tmap_3d(&tmQ, q, in_dtype, d_qk, h_q, total_q, qpt, p.group);
       if (st != FA_OK) return st;
-      // One split over packed K/V without a mask, chosen automatically: the
-      // persistent form walks a tile list held in shared memory, so the batch
-      // and its query pairs must fit that list.  Under a causal or window
-      // mask the tiles are short and unequal, and the non-persistent grid
-      // (dispatched m-major by the hardware's own greedy scheduler) measured
-      // faster than the persistent kernel's static deal.
+      // One split over packed K/V, chosen automatically: the persistent form
+      // walks a tile list held in shared memory, so the batch and its query
+      // pairs must fit that list, and it claims tiles from a ticket counter
+      // kept in the first bytes of the workspace (zeroed here, in stream
+      // order).  Without a workspace the non-persistent grid runs.
       const long long pairs = ceil_div(max_seqlen_q, 2 * qpt);
-      const bool persistent = kernel_sel == FA_KERNEL_AUTO && ns == 1 && !paged && !causal &&
-                              window_left < 0 && batch <= 128 && pairs <= kMaxUnitPairs &&
+      const bool has_sched = workspace != nullptr && aligned16(workspace) &&
+                             (workspace_bytes == (size_t)-1 || workspace_bytes >= kSchedBytes);
+      const bool persistent = kernel_sel == FA_KERNEL_AUTO && ns == 1 && !paged && has_sched &&
+                              batch <= 128 && pairs <= kMaxUnitPairs &&
                               (long long)batch * pairs <= kMaxUnits;
       if (persistent) {
         int sms = 0;
@@ -458,6 +459,8 @@ int fwd_impl(const void* q, const void* k, const void* v, const int* cu_seqlens_
         if (st != FA_OK) return st;
         const long long tiles = (long long)batch * pairs * h_kv;
         dim3 grid((unsigned)(tiles < sms ? tiles : sms), 1, 1);
+        p.sched = static_cast<int*>(workspace);
+        if (cudaMemsetAsync(p.sched, 0, sizeof(int), s) != cudaSuccess) return FA_ERR_CUDA;
         e = in_dtype == kFP16 ? launch_umma2p_fp16(d_qk, d_v, p, tmQ, tmK, tmV, grid, s)
                               : launch_umma2p_bf16(d_qk, d_v, p, tmQ, tmK, tmV, grid, s);
       } else {

@@ -19,6 +19,11 @@ constexpr int kMaxSplits = 128;
 // units held in shared memory, 7 bits of sequence and 9 of pair each.
 constexpr int kMaxUnits = 640;
 constexpr int kMaxUnitPairs = 512;
+// Slots of the ring through which its producer hands each claimed tile to the
+// MMA and softmax roles.
+constexpr int kTileRing = 4;
+// Workspace bytes of a one-split call: the persistent kernel's ticket counter.
+constexpr unsigned kSchedBytes = 16;
 constexpr int kMinPage = 32;                 // smallest page of a paged K/V cache
 constexpr int kMaxSub = kBlockN / kMinPage;  // page-sized loads per key block, at most
 
@@ -57,6 +62,7 @@ struct FwdParams {
   int page_size;    // 0: contiguous packed K/V addressed through cu_k
   int page_shift;   // log2(page_size)
   int num_sms;      // SMs of the device (0 if unknown)
+  int* sched;       // persistent kernel's tile ticket counter, zero at launch
 };
 
 struct SeqInfo {

@@ -14,7 +14,12 @@
 // length-aware schedule is the named follow-up.  This one first compacts the
 // tiles that exist (sequence, 256-row query pair) into a list ordered
 // longest first -- by key count without a mask, by query-pair index (the
-// causal work) with one -- and deals it out to the CTAs in snake order.
+// causal work) with one.  Each CTA starts on the tile of its own index and
+// claims every later one from a ticket counter in global memory when the tile
+// before it starts: the list goes out greedily, longest first, to whichever
+// CTA is free, and the claim's latency hides behind the tile's first loads.
+// The producer hands each claimed tile to the MMA and softmax roles through a
+// small ring in shared memory (full/empty barriers; -1 ends the walk).
 //
 // Per tile everything is as in the two-tile kernel (fa_umma2.cuh): two
 // 128-row query tiles A and B share each K/V block, the MMA warp alternates
@@ -40,9 +45,13 @@ template <int DT, int DQK, int DV, int KS, int VS>
 struct Umma2pCfg {
   using B = Umma2Cfg<DT, DQK, DV, KS, VS>;
   // Shared layout of the two-tile kernel, then: q_empty, o_free[2], the
-  // unit count and the unit list (b | m << 7, uint16).
+  // tile ring's full/empty barriers and slots, the unit count and the unit
+  // list (b | m << 7, uint16).
   static constexpr int OFF_BAR2 = B::OFF_FLAG + 16;
-  static constexpr int OFF_NUNITS = OFF_BAR2 + 24;
+  static constexpr int OFF_TRING_BAR = OFF_BAR2 + 24;               // full[R], empty[R]
+  static constexpr int OFF_TRING = OFF_TRING_BAR + 16 * kTileRing;  // decoded tiles [R]
+  static constexpr int TRING_SLOT = 64;
+  static constexpr int OFF_NUNITS = OFF_TRING + TRING_SLOT * kTileRing;
   static constexpr int OFF_UNITS = OFF_NUNITS + 8;
   static constexpr int SMEM = OFF_UNITS + 2 * kMaxUnits + 1024;
   // Register split (launch: 384 x 168): the producer and MMA roles carry the
@@ -57,22 +66,24 @@ struct Umma2pCfg {
   static_assert(KS * B::K_STAGE >= 4 * 129 * 4, "list scratch");
 };
 
-// Tile k of this CTA in the compacted list (snake order over the CTAs), or -1.
-__device__ __forceinline__ int unit_tile(int k, int n_tiles) {
-  const int G = gridDim.x;
-  const int c = blockIdx.x;
-  const int r = k * G + ((k & 1) ? (G - 1 - c) : c);
+// The tile a claim from the ticket counter stands for, or -1 once the list is
+// exhausted.  Tiles 0..G-1 are every CTA's first (its own index, no claim);
+// ticket t of the counter is tile G + t, so tiles go out in list order to
+// whichever CTA asks first.
+__device__ __forceinline__ int ticket_tile(int ticket, int n_tiles) {
+  const int r = (int)gridDim.x + ticket;
   return r < n_tiles ? r : -1;
 }
 
 // Everything about one tile that every role needs, computed the same way by
 // each of them.
 struct PTile {
-  int b, kh, m_blk;
+  int b, kh, m_blk;  // b < 0: the end of the walk
   SeqInfo sq;
   int q_start, nq_a, nq_b;
   int k0, k1, kb0, nblk;
 };
+static_assert(sizeof(PTile) <= 64, "tile ring slot");
 
 __device__ __forceinline__ void decode_ptile(const FwdParams& p, const uint16_t* units, int r,
                                              int qpt, PTile& t) {
@@ -200,6 +211,9 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t drain = o_done + 16;
   const uint32_t q_empty = sbase + CP::OFF_BAR2;
   const uint32_t o_free = q_empty + 8;              // [2]
+  const uint32_t tr_full = sbase + CP::OFF_TRING_BAR;  // [kTileRing]
+  const uint32_t tr_empty = tr_full + 8 * kTileRing;    // [kTileRing]
+  PTile* tring = reinterpret_cast<PTile*>(smem + CP::OFF_TRING);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
 
@@ -219,6 +233,11 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(p_ready + 8 * t, 128);
       mbar_init(o_done + 8 * t, 1);
       mbar_init(o_free + 8 * t, 128);
+    }
+    // a tile slot is released by the MMA thread and the eight softmax warps
+    for (int s = 0; s < kTileRing; ++s) {
+      mbar_init(tr_full + 8 * s, 1);
+      mbar_init(tr_empty + 8 * s, 9);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -289,22 +308,30 @@ __global__ void __launch_bounds__(384, 1)
           for (int pv = 0; pv < C::NPV; ++pv)
             tma_prefetch_l2_3d(&tmV, pv * C::PANEL_ELEMS, T.kh, T.sq.k0 + T.kb0);
         };
+        // Every CTA's first tile is its own index; each later one is claimed
+        // from the ticket counter when the tile before it starts, so the
+        // tiles (longest first) go to whichever CTA is free first.
+        int claimed = (int)blockIdx.x < n_tiles ? (int)blockIdx.x : -1;
         for (int k = 0; ok; ++k) {
-          const int r = unit_tile(k, n_tiles);
+          const int r = claimed;
+          int ticket = 0;
+          if (r >= 0) ticket = atomicAdd(p.sched, 1);  // read once this tile's Q is issued
+          PTile T = {};
+          if (r >= 0)
+            decode_ptile(p, units, r, qpt, T);
+          else
+            T.b = -1;
+          // hand the decoded tile (or the end mark) to the MMA and softmax roles
+          const int sl = k % kTileRing;
+          if (k >= kTileRing &&
+              !mbar_wait(tr_empty + 8 * sl, ((k / kTileRing) - 1) & 1, p.err, abort_flag))
+            break;
+          tring[sl] = T;
+          mbar_arrive(tr_full + 8 * sl);
           if (r < 0) break;
-          PTile T;
-          decode_ptile(p, units, r, qpt, T);
-          if (T.nblk == 0) continue;
-          {  // the next tile with work, prefetched into L2
-            for (int k2 = k + 1;; ++k2) {
-              const int r2 = unit_tile(k2, n_tiles);
-              if (r2 < 0) break;
-              PTile T2;
-              decode_ptile(p, units, r2, qpt, T2);
-              if (T2.nblk == 0) continue;
-              prefetch_tile(T2);
-              break;
-            }
+          if (T.nblk == 0) {
+            claimed = ticket_tile(ticket, n_tiles);
+            continue;
           }
           // K(0) first: its ring stage frees long before the old Q does
           if (!load_k(T, 0)) break;
@@ -318,6 +345,13 @@ __global__ void __launch_bounds__(384, 1)
               tma_load_3d(sbase + C::OFF_Q + (t * C::NPQ + pq) * C::PANEL, &tmQ, q_full,
                           pq * C::PANEL_ELEMS, T.kh * group, T.sq.q0 + T.q_start + t * qpt, pol_q);
           ++issued_q;
+          // the claimed next tile's Q and first K/V block into L2
+          claimed = ticket_tile(ticket, n_tiles);
+          if (claimed >= 0) {
+            PTile T2;
+            decode_ptile(p, units, claimed, qpt, T2);
+            if (T2.nblk > 0) prefetch_tile(T2);
+          }
           // K(1), V(0), K(2), V(1), ...: K one block ahead of V.
           for (int j = 1; j <= T.nblk; ++j) {
             if (j < T.nblk && !load_k(T, j)) {
@@ -354,57 +388,108 @@ __global__ void __launch_bounds__(384, 1)
                           smem_desc_sw128(v_addr + ks * C::UMMA_K * 128, C::PANEL, 1024),
                           C::IDESC_PV, (!first || ks > 0) ? 1u : 0u);
         };
-        // running counts: Q tiles, K and V blocks consumed, p_ready waits and
-        // O tiles per slot
-        int nq = 0, gk = 0, gv = 0;
-        int pc[2] = {0, 0}, od[2] = {0, 0};
+        // Running counts: Q tiles and K/V blocks consumed, ring entries read;
+        // per slot (bit t) the parity of its p_ready waits and O tiles, and
+        // whether it has held an O tile yet.
+        int nq = 0, gk = 0, gv = 0, kr = 0;
+        uint32_t pcb = 0, odb = 0, odv = 0;
         bool ok = true;
-        for (int k = 0; ok; ++k) {
-          const int r = unit_tile(k, n_tiles);
-          if (r < 0) break;
-          PTile T;
-          decode_ptile(p, units, r, qpt, T);
-          if (T.nblk == 0) continue;
-          const int ntiles = T.nq_b > 0 ? 2 : 1;
-          ok = mbar_wait(q_full, nq & 1, p.err, abort_flag) &&
-               mbar_wait(k_full + 8 * (gk % KS), (gk / KS) & 1, p.err, abort_flag);
-          if (!ok) break;
-          ++nq;
-          tc_fence_after();
-          for (int t = 0; t < ntiles; ++t) issue_s(t, gk % KS);
-          tc_commit(k_empty + 8 * (gk % KS));  // K(0) is free once both S(0) are done
+        auto read_ring = [&](PTile& X) {
+          const int sl = kr % kTileRing;
+          if (!mbar_wait(tr_full + 8 * sl, (kr / kTileRing) & 1, p.err, abort_flag)) return false;
+          X = tring[sl];
+          mbar_arrive(tr_empty + 8 * sl);
+          ++kr;
+          return true;
+        };
+        // S(0) of the next tile into slot t, once its Q and K(0) have landed
+        bool s0_ready = false;
+        auto issue_s0 = [&](int t) {
+          if (!s0_ready) {
+            if (!mbar_wait(q_full, nq & 1, p.err, abort_flag) ||
+                !mbar_wait(k_full + 8 * (gk % KS), (gk / KS) & 1, p.err, abort_flag))
+              return false;
+            tc_fence_after();
+            s0_ready = true;
+          }
+          issue_s(t, gk % KS);
+          return true;
+        };
+        // all S(0) of tile X are issued: K(0) frees once they are done
+        auto finish_s0 = [&](const PTile& X) {
+          tc_commit(k_empty + 8 * (gk % KS));
           ++gk;
-          if (T.nblk == 1) tc_commit(q_empty);  // the tile's last S MMAs are issued
+          ++nq;
+          s0_ready = false;
+          if (X.nblk == 1) tc_commit(q_empty);  // its only S MMAs are issued
+        };
+        PTile T;
+        ok = read_ring(T);
+        bool s0_done = false;  // T's S(0) went in behind the previous tile
+        while (ok && T.b >= 0) {
+          if (T.nblk == 0) {
+            ok = read_ring(T);
+            s0_done = false;
+            continue;
+          }
+          const int ntiles = T.nq_b > 0 ? 2 : 1;
+          if (!s0_done) {
+            for (int t = 0; ok && t < ntiles; ++t) ok = issue_s0(t);
+            if (!ok) break;
+            finish_s0(T);
+          }
+          // The next ring entry is read at the last block; when it has key
+          // blocks, its S(0) goes into each slot right behind that slot's
+          // last PV (MMAs run in issue order, so S may overwrite P then), and
+          // the softmax warps find it ready when their epilogue ends.  Only
+          // one entry ahead: the producer can always publish it.
+          PTile N;
+          N.b = -1;
+          int n_ntiles = 0;
           for (int j = 0; ok && j < T.nblk; ++j) {
             const int vst = gv % VS;
+            const bool last = j + 1 == T.nblk;
             for (int t = 0; t < ntiles; ++t) {
-              ok = mbar_wait(p_ready + 8 * t, pc[t] & 1, p.err, abort_flag);
-              ++pc[t];
+              ok = mbar_wait(p_ready + 8 * t, (pcb >> t) & 1, p.err, abort_flag);
+              pcb ^= 1u << t;
               if (ok && t == 0) ok = mbar_wait(v_full + 8 * vst, (gv / VS) & 1, p.err, abort_flag);
-              if (ok && t == 0 && j + 1 < T.nblk)
+              if (ok && t == 0 && !last)
                 ok = mbar_wait(k_full + 8 * (gk % KS), (gk / KS) & 1, p.err, abort_flag);
               // the previous tile's O in this slot has been read out of TMEM
-              if (ok && j == 0 && od[t] > 0)
-                ok = mbar_wait(o_free + 8 * t, (od[t] - 1) & 1, p.err, abort_flag);
+              if (ok && j == 0 && ((odv >> t) & 1))
+                ok = mbar_wait(o_free + 8 * t, ((odb >> t) & 1) ^ 1u, p.err, abort_flag);
               if (!ok) break;
               tc_fence_after();
               issue_pv(t, vst, j == 0);
-              if (j + 1 < T.nblk) {
+              if (!last) {
                 issue_s(t, gk % KS);
               } else {
                 tc_commit(o_done + 8 * t);
-                ++od[t];
+                odb ^= 1u << t;
+                odv |= 1u << t;
+                if (t == 0) {
+                  ok = read_ring(N);
+                  if (!ok) break;
+                  n_ntiles = (N.b >= 0 && N.nblk > 0) ? (N.nq_b > 0 ? 2 : 1) : 0;
+                }
+                if (t < n_ntiles && !(ok = issue_s0(t))) break;
               }
             }
             if (!ok) break;
+            if (last)  // a slot this tile left idle
+              for (int t = ntiles; ok && t < n_ntiles; ++t) ok = issue_s0(t);
+            if (!ok) break;
             tc_commit(v_empty + 8 * vst);
             ++gv;
-            if (j + 1 < T.nblk) {
+            if (!last) {
               tc_commit(k_empty + 8 * (gk % KS));
               ++gk;
             }
             if (j + 2 == T.nblk) tc_commit(q_empty);  // S(nblk-1) of both tiles issued
+            if (last && n_ntiles > 0) finish_s0(N);
           }
+          s0_done = n_ntiles > 0;
+          T = N;
         }
         tc_commit(drain);
         mbar_wait(drain, 0, nullptr, nullptr);
@@ -442,10 +527,13 @@ __global__ void __launch_bounds__(384, 1)
     int sc = 0, od = 0;  // s_full waits and O tiles of this slot
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int rr = unit_tile(k, n_tiles);
-      if (rr < 0) break;
-      PTile T;
-      decode_ptile(p, units, rr, qpt, T);
+      const int sl = k % kTileRing;
+      ok = mbar_wait(tr_full + 8 * sl, (k / kTileRing) & 1, p.err, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const PTile T = tring[sl];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tr_empty + 8 * sl);
+      if (T.b < 0) break;
       const int nq = t == 0 ? T.nq_a : T.nq_b;
       if (nq <= 0) continue;
       const int nrows = nq * group;
@@ -545,23 +633,27 @@ __global__ void __launch_bounds__(384, 1)
         lse_v = (m_run + __log2f(l_run)) * 0.69314718055994531f;
       }
       const int tok = T.sq.q0 + i;
+      // O out of TMEM in one load, released, then scaled and stored
+      uint32_t o[DV];
+      if (warp_active && T.nblk > 0) {
+        if constexpr (DV == 128)
+          tmem_ld128(o_addr, o);
+        else
+          tmem_ld64(o_addr, o);
+      } else {
 #pragma unroll
-      for (int c = 0; c < DV / 32; ++c) {
-        uint32_t o[32];
-        if (warp_active && T.nblk > 0) {
-          tmem_ld32(o_addr + 32 * c, o);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
-        }
-        if (warp_active && row_ok)
-          store_o<32>(p.out, ((size_t)tok * p.h_q + h) * DV + c * 32,
-                      reinterpret_cast<const float*>(o), inv, p.out_dtype);
+        for (int e = 0; e < DV; ++e) o[e] = 0u;
       }
       if (T.nblk > 0) {
         // O has been read out of TMEM: the next tile's first PV may overwrite it
         tc_fence_before();
         mbar_arrive(o_free + 8 * t);
+      }
+      if (warp_active && row_ok) {
+#pragma unroll
+        for (int c = 0; c < DV / 32; ++c)
+          store_o<32>(p.out, ((size_t)tok * p.h_q + h) * DV + c * 32,
+                      reinterpret_cast<const float*>(o + 32 * c), inv, p.out_dtype);
       }
       if (warp_active && row_ok && p.lse != nullptr) p.lse[(size_t)h * p.total_q + tok] = lse_v;
     }

@@ -450,8 +450,8 @@ def main():
             # the persistent form: one split, packed K/V, a workspace, tile list fits
             qpt = 128 // (inp.h_q // inp.h_kv)
             pairs = -(-inp.max_seqlen_q // (2 * qpt))
-            persistent = (ns == 1 and not paged and ws is not None and inp.batch <= 128
-                          and pairs <= 512 and inp.batch * pairs <= 640)
+            persistent = (ns == 1 and not paged and ws is not None and out.data_ptr() % 32 == 0
+                          and inp.batch <= 128 and pairs <= 512 and inp.batch * pairs <= 640)
             kern_tag = "umma2p_splitkv" if persistent else "umma2_splitkv"
         else:
             kern_tag = "umma_splitkv"

@@ -444,14 +444,17 @@ int fwd_impl(const void* q, const void* k, const void* v, const int* cu_seqlens_
       if (st != FA_OK) return st;
       // One split over packed K/V, chosen automatically: the persistent form
       // walks a tile list held in shared memory, so the batch and its query
-      // pairs must fit that list, and it claims tiles from a ticket counter
-      // kept in the first bytes of the workspace (zeroed here, in stream
-      // order).  Without a workspace the non-persistent grid runs.
+      // pairs must fit that list; it claims tiles from a ticket counter kept
+      // in the first bytes of the workspace (zeroed here, in stream order);
+      // and it writes O rows with 32-byte stores, so out must be 32-byte
+      // aligned (rows are then too: h_q * d_v * element size is a multiple
+      // of 32).  Otherwise the non-persistent grid runs.
       const long long pairs = ceil_div(max_seqlen_q, 2 * qpt);
       const bool has_sched = workspace != nullptr && aligned16(workspace) &&
                              (workspace_bytes == (size_t)-1 || workspace_bytes >= kSchedBytes);
+      const bool out32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
       const bool persistent = kernel_sel == FA_KERNEL_AUTO && ns == 1 && !paged && has_sched &&
-                              batch <= 128 && pairs <= kMaxUnitPairs &&
+                              out32 && batch <= 128 && pairs <= kMaxUnitPairs &&
                               (long long)batch * pairs <= kMaxUnits;
       if (persistent) {
         int sms = 0;

@@ -134,10 +134,17 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, int out_dtype) {
 // N consecutive output elements (already normalised, times `scale`) at
 // element index `elem` of O: 16-bit types as 2N bytes (round to nearest), e4m3
 // as N bytes (round to nearest even, saturating to +-448).  N is 2, 4, 8 or
-// 32; the address is aligned to the store width (2N or N bytes).
-template <int N>
+// 32; the address is aligned to the store width (2N or N bytes).  WIDE (N = 32
+// only): 32-byte stores, the address 32-byte aligned.
+__device__ __forceinline__ void st_global_32B(void* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+template <int N, bool WIDE = false>
 __device__ __forceinline__ void store_o(void* out, size_t elem, const float* f, float scale,
                                         int out_dtype) {
+  static_assert(!WIDE || N == 32, "wide stores take 32 values");
   static_assert(N == 2 || N == 4 || N == 8 || N == 32, "store width");
   if (out_dtype == kE4M3) {
     uint8_t* dst = static_cast<uint8_t*>(out) + elem;
@@ -156,6 +163,8 @@ __device__ __forceinline__ void store_o(void* out, size_t elem, const float* f, 
       *reinterpret_cast<uint32_t*>(dst) = w[0];
     } else if constexpr (N == 8) {
       *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    } else if constexpr (WIDE) {
+      st_global_32B(dst, w);
     } else {
 #pragma unroll
       for (int i = 0; i < N / 16; ++i)
@@ -170,6 +179,9 @@ __device__ __forceinline__ void store_o(void* out, size_t elem, const float* f, 
       *reinterpret_cast<uint32_t*>(dst) = w[0];
     } else if constexpr (N == 4) {
       *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    } else if constexpr (WIDE) {
+      st_global_32B(dst, w);
+      st_global_32B(dst + 32, w + 8);
     } else {
 #pragma unroll
       for (int i = 0; i < N / 8; ++i)

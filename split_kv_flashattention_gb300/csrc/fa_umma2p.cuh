@@ -652,8 +652,8 @@ __global__ void __launch_bounds__(384, 1)
       if (warp_active && row_ok) {
 #pragma unroll
         for (int c = 0; c < DV / 32; ++c)
-          store_o<32>(p.out, ((size_t)tok * p.h_q + h) * DV + c * 32,
-                      reinterpret_cast<const float*>(o + 32 * c), inv, p.out_dtype);
+          store_o<32, true>(p.out, ((size_t)tok * p.h_q + h) * DV + c * 32,
+                            reinterpret_cast<const float*>(o + 32 * c), inv, p.out_dtype);
       }
       if (warp_active && row_ok && p.lse != nullptr) p.lse[(size_t)h * p.total_q + tok] = lse_v;
     }

@@ -21,10 +21,11 @@ def device():
 
 
 def run_gpu(inp, scale=0.0, causal=False, window_left=-1, num_splits=0, flags=0,
-            with_lse=True, guard_rows=0, out_dtype=None, ws_guard=0):
+            with_lse=True, guard_rows=0, out_dtype=None, ws_guard=0, out_offset=0):
     """Runs fa_fwd_splitkv_ex on `inp` (workloads.Inputs).  Output rows past
     the packed queries (guard_rows of them) and ws_guard floats past the
-    workspace are filled with NaN sentinels and must stay untouched."""
+    workspace are filled with NaN sentinels and must stay untouched.  O starts
+    out_offset bytes into its allocation; the bytes before it must stay NaN."""
     dev = device()
     q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
     cq, ck = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev)
@@ -35,7 +36,10 @@ def run_gpu(inp, scale=0.0, causal=False, window_left=-1, num_splits=0, flags=0,
         q = qpad
     if out_dtype is None:
         out_dtype = torch.bfloat16 if inp.dtype == "e4m3" else q.dtype
-    out = torch.full((total_q, inp.h_q, inp.d_v), float("nan"), dtype=out_dtype, device=dev)
+    n_out = total_q * inp.h_q * inp.d_v
+    pre = out_offset // torch.empty((), dtype=out_dtype).element_size()
+    out_buf = torch.full((pre + n_out,), float("nan"), dtype=out_dtype, device=dev)
+    out = out_buf[pre:].view(total_q, inp.h_q, inp.d_v)
     lse = (torch.full((inp.h_q, total_q), float("nan"), dtype=torch.float32, device=dev)
            if with_lse else None)
     ns_bytes = fa.fa_fwd_splitkv_workspace_size(inp.batch, inp.max_seqlen_q, inp.h_q, inp.h_kv,
@@ -55,6 +59,8 @@ def run_gpu(inp, scale=0.0, causal=False, window_left=-1, num_splits=0, flags=0,
     assert err == 0, fa.fa_status_string(err)
     if ws is not None and ws_guard:
         assert torch.isnan(ws[ns_bytes // 4:]).all(), "workspace guard overwritten"
+    if pre:
+        assert torch.isnan(out_buf[:pre].float()).all(), "bytes before O overwritten"
     return out.float().cpu().numpy(), (lse.cpu().numpy() if lse is not None else None)
 
 

@@ -465,6 +465,20 @@ def test_persistent_prefill_q_and_k_lengths_differ(causal):
     assert_close(inp, out, lse, o_ref, l_ref)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_persistent_prefill_out_not_32_byte_aligned(causal):
+    """The persistent kernel writes O rows in 32-byte pieces, so an O that
+    starts 16 bytes past a 32-byte boundary takes the non-persistent two-tile
+    kernel: same bits, and nothing written before O."""
+    lens = [700, 300, 520]
+    inp = _quarter_v(make_inputs(lens, lens, 4, 2, 128, 128, "bf16", seed=45))
+    out, lse = run_gpu(inp, causal=causal, num_splits=1)
+    o_ref, l_ref = reference(inp, 0.0, causal)
+    assert_close(inp, out, lse, o_ref, l_ref)
+    out2, lse2 = run_gpu(inp, causal=causal, num_splits=1, out_offset=16)
+    assert np.array_equal(out, out2, equal_nan=True) and np.array_equal(lse, lse2, equal_nan=True)
+
+
 def test_persistent_prefill_running_max_jumps():
     lens = [700, 300, 520]
     inp = _quarter_v(make_inputs(lens, lens, 2, 2, 128, 128, "bf16", seed=44))

@@ -128,77 +128,9 @@ __global__ void __launch_bounds__(384, 1)
   pdl_wait();  // the previous kernel in the stream is complete from here on
   if (__syncthreads_or(timed_out_before(p.err))) return;
 
-  // ---- the tile list: units (sequence, query pair) that exist, longest first
-  uint16_t* units = reinterpret_cast<uint16_t*>(smem + CP::OFF_UNITS);
-  int* n_units_s = reinterpret_cast<int*>(smem + CP::OFF_NUNITS);
-  {
-    int* s_pairs = reinterpret_cast<int*>(smem + CP::OFF_SCRATCH);  // [128]
-    int* s_keys = s_pairs + 128;                                     // [128]
-    int* s_order = s_keys + 128;                                     // [128] rank -> sequence
-    int* s_off = s_order + 128;                                      // [129]
-    for (int bb = threadIdx.x; bb < p.batch; bb += blockDim.x) {
-      SeqInfo s;
-      int pr = 0, key = 0;
-      if (load_seq(p, bb, s)) {
-        pr = min((s.lq + 2 * qpt - 1) / (2 * qpt), kMaxUnitPairs);
-        key = s.lk;
-      } else if (blockIdx.x == 0) {
-        record_error(p.err, kErrDeviceArg);
-      }
-      s_pairs[bb] = pr;
-      s_keys[bb] = key;
-    }
-    __syncthreads();
-    const bool masked = p.causal || p.window_left >= 0;
-    if (!masked) {
-      // sequences by key count, longest first (ties by index)
-      for (int bb = threadIdx.x; bb < p.batch; bb += blockDim.x) {
-        int rk = 0;
-        for (int c = 0; c < p.batch; ++c)
-          rk += (s_keys[c] > s_keys[bb]) | ((s_keys[c] == s_keys[bb]) & (c < bb));
-        s_order[rk] = bb;
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        int acc = 0;
-        for (int rk = 0; rk < p.batch; ++rk) {
-          s_off[rk] = acc;
-          acc += s_pairs[s_order[rk]];
-        }
-        s_off[p.batch] = acc;
-        *n_units_s = min(acc, kMaxUnits);
-      }
-      __syncthreads();
-      for (int rk = threadIdx.x; rk < p.batch; rk += blockDim.x) {
-        const int bb = s_order[rk];
-        const int pr = s_pairs[bb];
-        for (int m = 0; m < pr; ++m) {
-          const int at = s_off[rk] + m;
-          if (at < kMaxUnits) units[at] = (uint16_t)(bb | ((pr - 1 - m) << 7));
-        }
-      }
-    } else if (warp == 0) {
-      // query pairs from the last (most keys under the mask) down, sequences
-      // in order within a level
-      int maxp = 0;
-      for (int bb = lane; bb < p.batch; bb += 32) maxp = max(maxp, s_pairs[bb]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) maxp = max(maxp, __shfl_xor_sync(0xffffffffu, maxp, o));
-      int n = 0;
-      for (int m = maxp - 1; m >= 0; --m) {
-        for (int base = 0; base < p.batch; base += 32) {
-          const int bb = base + lane;
-          const bool on = bb < p.batch && s_pairs[bb] > m;
-          const unsigned bal = __ballot_sync(0xffffffffu, on);
-          const int at = n + __popc(bal & ((1u << lane) - 1u));
-          if (on && at < kMaxUnits) units[at] = (uint16_t)(bb | (m << 7));
-          n += __popc(bal);
-        }
-      }
-      if (lane == 0) *n_units_s = min(n, kMaxUnits);
-    }
-  }
-
+  // Barriers (thread 0) and TMEM (warp 1) first: they do not depend on the
+  // tile list, and their latency then hides behind the cu_seqlens loads that
+  // warps 4-11 make for the list.
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t q_full = bar0;
   const uint32_t k_full = bar0 + 8;                // [KS]
@@ -247,6 +179,79 @@ __global__ void __launch_bounds__(384, 1)
     tmem_alloc(sbase + C::OFF_TMEM_SLOT, C::TMEM_COLS);
     tmem_relinquish();
   }
+
+  // ---- the tile list: units (sequence, query pair) that exist, longest first
+  uint16_t* units = reinterpret_cast<uint16_t*>(smem + CP::OFF_UNITS);
+  int* n_units_s = reinterpret_cast<int*>(smem + CP::OFF_NUNITS);
+  {
+    int* s_pairs = reinterpret_cast<int*>(smem + CP::OFF_SCRATCH);  // [128]
+    int* s_keys = s_pairs + 128;                                     // [128]
+    int* s_order = s_keys + 128;                                     // [128] rank -> sequence
+    int* s_off = s_order + 128;                                      // [129]
+    const int lt = (int)threadIdx.x - 128;  // list builders: warps 4-11 (batch <= 128)
+    for (int bb = lt; bb >= 0 && bb < p.batch; bb += blockDim.x - 128) {
+      SeqInfo s;
+      int pr = 0, key = 0;
+      if (load_seq(p, bb, s)) {
+        pr = min((s.lq + 2 * qpt - 1) / (2 * qpt), kMaxUnitPairs);
+        key = s.lk;
+      } else if (blockIdx.x == 0) {
+        record_error(p.err, kErrDeviceArg);
+      }
+      s_pairs[bb] = pr;
+      s_keys[bb] = key;
+    }
+    __syncthreads();
+    const bool masked = p.causal || p.window_left >= 0;
+    if (!masked) {
+      // sequences by key count, longest first (ties by index)
+      for (int bb = lt; bb >= 0 && bb < p.batch; bb += blockDim.x - 128) {
+        int rk = 0;
+        for (int c = 0; c < p.batch; ++c)
+          rk += (s_keys[c] > s_keys[bb]) | ((s_keys[c] == s_keys[bb]) & (c < bb));
+        s_order[rk] = bb;
+      }
+      __syncthreads();
+      if (lt == 0) {
+        int acc = 0;
+        for (int rk = 0; rk < p.batch; ++rk) {
+          s_off[rk] = acc;
+          acc += s_pairs[s_order[rk]];
+        }
+        s_off[p.batch] = acc;
+        *n_units_s = min(acc, kMaxUnits);
+      }
+      __syncthreads();
+      for (int rk = lt; rk >= 0 && rk < p.batch; rk += blockDim.x - 128) {
+        const int bb = s_order[rk];
+        const int pr = s_pairs[bb];
+        for (int m = 0; m < pr; ++m) {
+          const int at = s_off[rk] + m;
+          if (at < kMaxUnits) units[at] = (uint16_t)(bb | ((pr - 1 - m) << 7));
+        }
+      }
+    } else if (warp == 4) {
+      // query pairs from the last (most keys under the mask) down, sequences
+      // in order within a level
+      int maxp = 0;
+      for (int bb = lane; bb < p.batch; bb += 32) maxp = max(maxp, s_pairs[bb]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) maxp = max(maxp, __shfl_xor_sync(0xffffffffu, maxp, o));
+      int n = 0;
+      for (int m = maxp - 1; m >= 0; --m) {
+        for (int base = 0; base < p.batch; base += 32) {
+          const int bb = base + lane;
+          const bool on = bb < p.batch && s_pairs[bb] > m;
+          const unsigned bal = __ballot_sync(0xffffffffu, on);
+          const int at = n + __popc(bal & ((1u << lane) - 1u));
+          if (on && at < kMaxUnits) units[at] = (uint16_t)(bb | (m << 7));
+          n += __popc(bal);
+        }
+      }
+      if (lane == 0) *n_units_s = min(n, kMaxUnits);
+    }
+  }
+
   tc_fence_before();
   __syncthreads();  // also publishes the tile list (and frees the scratch)
   tc_fence_after();
@@ -314,8 +319,6 @@ __global__ void __launch_bounds__(384, 1)
         int claimed = (int)blockIdx.x < n_tiles ? (int)blockIdx.x : -1;
         for (int k = 0; ok; ++k) {
           const int r = claimed;
-          int ticket = 0;
-          if (r >= 0) ticket = atomicAdd(p.sched, 1);  // read once this tile's Q is issued
           PTile T = {};
           if (r >= 0)
             decode_ptile(p, units, r, qpt, T);
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive(tr_full + 8 * sl);
           if (r < 0) break;
           if (T.nblk == 0) {
-            claimed = ticket_tile(ticket, n_tiles);
+            claimed = ticket_tile(atomicAdd(p.sched, 1), n_tiles);
             continue;
           }
           // K(0) first: its ring stage frees long before the old Q does
@@ -345,13 +348,6 @@ __global__ void __launch_bounds__(384, 1)
               tma_load_3d(sbase + C::OFF_Q + (t * C::NPQ + pq) * C::PANEL, &tmQ, q_full,
                           pq * C::PANEL_ELEMS, T.kh * group, T.sq.q0 + T.q_start + t * qpt, pol_q);
           ++issued_q;
-          // the claimed next tile's Q and first K/V block into L2
-          claimed = ticket_tile(ticket, n_tiles);
-          if (claimed >= 0) {
-            PTile T2;
-            decode_ptile(p, units, claimed, qpt, T2);
-            if (T2.nblk > 0) prefetch_tile(T2);
-          }
           // K(1), V(0), K(2), V(1), ...: K one block ahead of V.
           for (int j = 1; j <= T.nblk; ++j) {
             if (j < T.nblk && !load_k(T, j)) {
@@ -362,6 +358,15 @@ __global__ void __launch_bounds__(384, 1)
               ok = false;
               break;
             }
+          }
+          // This tile's loads are all issued: claim the next one now, so that
+          // no CTA holds a tile it will not start for a while, and bring its
+          // Q and first K/V block into L2.
+          claimed = ticket_tile(atomicAdd(p.sched, 1), n_tiles);
+          if (claimed >= 0) {
+            PTile T2;
+            decode_ptile(p, units, claimed, qpt, T2);
+            if (T2.nblk > 0) prefetch_tile(T2);
           }
         }
       }

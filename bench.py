@@ -115,9 +115,12 @@ def prefill_secondary(fa, dev, steps, warmup):
         lse = torch.empty((inp.h_q, inp.q.shape[0]), dtype=torch.float32, device=dev)
         cq, ck = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev)
         stream = torch.cuda.current_stream(dev)
+        ws_bytes = fa.fa_fwd_splitkv_workspace_size(inp.batch, inp.max_seqlen_q, inp.h_q, inp.h_kv,
+                                                   inp.d_v, 0)
+        ws = torch.empty(max(ws_bytes, 16) // 4, dtype=torch.float32, device=dev) if ws_bytes else None
 
         def step():
-            fa.fa_fwd_splitkv_ex(inp.q, inp.k, inp.v, cq, ck, inp.max_seqlen_q, out, lse, None,
+            fa.fa_fwd_splitkv_ex(inp.q, inp.k, inp.v, cq, ck, inp.max_seqlen_q, out, lse, ws,
                                  0.0, causal, -1, 0, None, None, None, 0, stream)
         for _ in range(warmup):
             step()

@@ -15,11 +15,12 @@
 // tiles that exist (sequence, 256-row query pair) into a list ordered
 // longest first -- by key count without a mask, by query-pair index (the
 // causal work) with one.  Each CTA starts on the tile of its own index and
-// claims every later one from a ticket counter in global memory when the tile
-// before it starts: the list goes out greedily, longest first, to whichever
-// CTA is free, and the claim's latency hides behind the tile's first loads.
-// The producer hands each claimed tile to the MMA and softmax roles through a
-// small ring in shared memory (full/empty barriers; -1 ends the walk).
+// claims every later one from a ticket counter in global memory once the
+// current tile's loads are all issued: the list goes out greedily, longest
+// first, to whichever CTA is free, and no CTA holds a tile it will not start
+// for a while.  The producer hands each decoded tile to the MMA and softmax
+// roles through a small ring in shared memory (full/empty barriers; b < 0
+// ends the walk).
 //
 // Per tile everything is as in the two-tile kernel (fa_umma2.cuh): two
 // 128-row query tiles A and B share each K/V block, the MMA warp alternates
@@ -28,7 +29,10 @@
 // keep running phase counts; two barriers are added: q_empty (the MMA warp's
 // commit after a tile's last S MMAs, so the producer may load the next Q) and
 // o_free[t] (the softmax warps' arrival once they have read a tile's O out of
-// TMEM, so the next tile's first PV may overwrite it).
+// TMEM, so the next tile's first PV may overwrite it).  At a tile's last
+// block the MMA warp issues the next tile's S(0) into each slot right behind
+// that slot's last PV, so the softmax warps find it ready when their
+// epilogue ends.
 #pragma once
 
 #include <cuda.h>

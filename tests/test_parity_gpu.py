@@ -181,6 +181,73 @@ def test_cuda_graph_replay_matches_eager():
     assert torch.equal(out, eager[0]) and torch.equal(lse, eager[1])
 
 
+def _prefill_buffers(inp, dev):
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    cq, ck = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev)
+    out = torch.empty((q.shape[0], inp.h_q, inp.d_v), dtype=q.dtype, device=dev)
+    lse = torch.empty((inp.h_q, q.shape[0]), dtype=torch.float32, device=dev)
+    nbytes = fa.fa_fwd_splitkv_workspace_size(inp.batch, inp.max_seqlen_q, inp.h_q, inp.h_kv,
+                                              inp.d_v, 1)
+    ws = torch.empty(max(nbytes, 16) // 4, dtype=torch.float32, device=dev)
+    return q, k, v, cq, ck, out, lse, ws
+
+
+def test_cuda_graph_replay_persistent_prefill():
+    """The persistent kernel's tile counter is zeroed by a memset in the
+    call's own stream order, so a captured call replays correctly: every
+    replay claims the whole tile list again."""
+    lens = [700, 300, 520]
+    inp = _quarter_v(make_inputs(lens, lens, 4, 2, 128, 128, "bf16", seed=46))
+    dev = torch.device("cuda:0")
+    q, k, v, cq, ck, out, lse, ws = _prefill_buffers(inp, dev)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, inp.max_seqlen_q, out, lse, ws, causal=True,
+                             num_splits=1, stream=s)
+    s.synchronize()
+    eager = out.clone(), lse.clone()
+    o_ref, l_ref = reference(inp, 0.0, True)
+    assert_close(inp, eager[0].float().cpu().numpy(), eager[1].cpu().numpy(), o_ref, l_ref)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, inp.max_seqlen_q, out, lse, ws, causal=True,
+                             num_splits=1, stream=s)
+    for _ in range(3):
+        out.zero_()
+        lse.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager[0]) and torch.equal(lse, eager[1])
+    assert fa.fa_get_device_error(clear=True) == 0
+
+
+def test_persistent_prefill_two_streams_own_workspaces():
+    """Two persistent prefills in flight at once on two streams, each with its
+    own workspace (so its own tile counter): both match their eager results."""
+    dev = torch.device("cuda:0")
+    runs = []
+    for seed, lens in ((47, [900, 260, 1100]), (48, [513, 2047, 64, 300])):
+        inp = _quarter_v(make_inputs(lens, lens, 8, 2, 128, 128, "bf16", seed=seed))
+        bufs = _prefill_buffers(inp, dev)
+        q, k, v, cq, ck, out, lse, ws = bufs
+        fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, inp.max_seqlen_q, out, lse, ws, num_splits=1)
+        torch.cuda.synchronize()
+        runs.append((inp, bufs, out.clone(), lse.clone()))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for _ in range(3):
+        for (inp, (q, k, v, cq, ck, out, lse, ws), _, _), st in zip(runs, streams):
+            out.zero_()
+            lse.zero_()
+        torch.cuda.synchronize()
+        for (inp, (q, k, v, cq, ck, out, lse, ws), _, _), st in zip(runs, streams):
+            fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, inp.max_seqlen_q, out, lse, ws, num_splits=1,
+                                 stream=st)
+        torch.cuda.synchronize()
+        for inp, (q, k, v, cq, ck, out, lse, ws), o0, l0 in runs:
+            assert torch.equal(out, o0) and torch.equal(lse, l0)
+    assert fa.fa_get_device_error(clear=True) == 0
+
+
 def test_partial_then_combine_equals_single_call():
     inp = workload("long_decode", kv=3000, h=4)
     a_out, a_lse = run_gpu(inp, num_splits=5)

@@ -231,6 +231,8 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_TAGS = {1: "simt_splitkv", 2: "umma_splitkv", 3: "umma2_splitkv", 4: "umma2p_splitkv"}
+
 KERNEL_SOURCES = {
     "simt_splitkv": ("fa_simt.cuh", "fa_simt_launch.cuh", "fa_simt_bf16.cu",
                      "fa_simt_bf16_ordered.cu", "fa_common.cuh", "fa_ptx.cuh", "fa_convert.cuh"),
@@ -444,23 +446,6 @@ def main():
         dk = torch.tensor([inp.descale_k], dtype=torch.float32, device=dev)
         dv = torch.tensor([inp.descale_v], dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    rows = inp.max_seqlen_q * (inp.h_q // inp.h_kv)
-    simt_rows = 2 if (inp.dtype == "e4m3" and inp.d_qk == 192) else 4
-    if args.kernel == "auto":
-        if rows <= simt_rows:
-            kern_tag = "simt_splitkv"
-        elif rows > 128 and inp.dtype != "e4m3" and inp.d_qk <= 128:
-            # the persistent form: one split, packed K/V, a workspace, tile list fits
-            qpt = 128 // (inp.h_q // inp.h_kv)
-            pairs = -(-inp.max_seqlen_q // (2 * qpt))
-            persistent = (ns == 1 and not paged and ws is not None and out.data_ptr() % 32 == 0
-                          and inp.batch <= 128 and pairs <= 512 and inp.batch * pairs <= 640)
-            kern_tag = "umma2p_splitkv" if persistent else "umma2_splitkv"
-        else:
-            kern_tag = "umma_splitkv"
-    else:
-        kern_tag = {"simt": "simt_splitkv", "umma": "umma_splitkv", "umma2": "umma2_splitkv"}[args.kernel]
-
     def call(flags):
         if paged:
             fa.fa_fwd_splitkv_paged(q, kc, vc, cq, sk, bt, inp.max_seqlen_q, out, lse, ws, 0.0,
@@ -484,6 +469,10 @@ def main():
     torch.cuda.synchronize(dev)
     if fa.fa_get_device_error(clear=True) != 0:
         raise RuntimeError("device error during warm-up")
+    # the partial kernel the library chose (the last call above enqueued it)
+    partial()
+    kern_tag = KERNEL_TAGS[fa.fa_debug_last_kernel()]
+    torch.cuda.synchronize(dev)
 
     # Timed region: K whole steps (partial + combine, as one call makes them,
     # so the combine's programmatic launch overlaps the partial's tail).

@@ -248,6 +248,22 @@ FA_API int fa_debug_split_ranges(const int* cu_seqlens_q, const int* cu_seqlens_
  * Returns FA_ERR_INVALID_ARG for a timeout outside 1..10000 ms. */
 FA_API int fa_debug_wait_timeout(unsigned int timeout_ms, void* stream);
 
+/* Partial kernels a forward call can launch, as fa_debug_last_kernel reports
+ * them (these are not flag values). */
+typedef enum {
+  FA_KID_NONE = 0,             /* no partial kernel launched                      */
+  FA_KID_SIMT = 1,             /* CUDA-core streaming kernel                      */
+  FA_KID_UMMA = 2,             /* tcgen05 kernel, one 128-row tile per CTA        */
+  FA_KID_UMMA2 = 3,            /* tcgen05 kernel, two 128-row tiles per CTA       */
+  FA_KID_UMMA2_PERSISTENT = 4  /* its persistent form (chosen by AUTO only)       */
+} fa_kernel_id;
+
+/* Test hook (no counterpart in the pages): the partial kernel that the calling
+ * thread's most recent fa_fwd_splitkv* call enqueued, recorded on the host at
+ * launch (fa_kernel_id); FA_KID_NONE if that call enqueued none (an argument
+ * error, FA_RUN_COMBINE_ONLY, or no sequence). */
+FA_API int fa_debug_last_kernel(void);
+
 /* Sticky device error word of the current device (FA_OK if none).  Waits
  * for the device to finish its work.  clear != 0 resets the word. */
 FA_API int fa_get_device_error(int clear);

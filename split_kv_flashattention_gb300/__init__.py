@@ -20,6 +20,8 @@ import torch
 __all__ = [
     "FaError", "FaLibraryMissing", "library", "fa_fwd_splitkv_ex", "fa_fwd_splitkv",
     "fa_fwd_splitkv_workspace_size", "fa_plan", "fa_debug_split_ranges", "fa_debug_wait_timeout",
+    "fa_debug_last_kernel", "FA_KID_NONE", "FA_KID_SIMT", "FA_KID_UMMA", "FA_KID_UMMA2",
+    "FA_KID_UMMA2_PERSISTENT",
     "fa_get_device_error", "fa_status_string", "fa_version", "forward",
     "FA_KERNEL_AUTO", "FA_KERNEL_SIMT", "FA_KERNEL_UMMA", "FA_KERNEL_UMMA2", "FA_RUN_PARTIAL_ONLY",
     "FA_RUN_COMBINE_ONLY", "DTYPE_CODES", "fa_fwd_splitkv_noalloc", "NOALLOC_SCRATCH_BYTES",
@@ -30,11 +32,13 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libf
 
 FA_KERNEL_AUTO, FA_KERNEL_SIMT, FA_KERNEL_UMMA, FA_KERNEL_UMMA2 = 0, 1, 2, 3
 FA_RUN_PARTIAL_ONLY, FA_RUN_COMBINE_ONLY = 4, 8
+FA_KID_NONE, FA_KID_SIMT, FA_KID_UMMA, FA_KID_UMMA2, FA_KID_UMMA2_PERSISTENT = 0, 1, 2, 3, 4
 DTYPE_CODES = {torch.bfloat16: 0, torch.float16: 1, torch.float8_e4m3fn: 2}
 EXPORTED = (
     "fa_fwd_splitkv_ex", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_plan",
     "fa_debug_split_ranges", "fa_get_device_error", "fa_status_string", "fa_version",
     "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_paged", "fa_debug_wait_timeout",
+    "fa_debug_last_kernel",
 )
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -89,6 +93,8 @@ def library() -> ctypes.CDLL:
     lib.fa_debug_split_ranges.argtypes = [_vp, _vp] + [_c_int] * 6 + [_vp, _vp]
     lib.fa_debug_wait_timeout.restype = _c_int
     lib.fa_debug_wait_timeout.argtypes = [ctypes.c_uint, _vp]
+    lib.fa_debug_last_kernel.restype = _c_int
+    lib.fa_debug_last_kernel.argtypes = []
     lib.fa_get_device_error.restype = _c_int
     lib.fa_get_device_error.argtypes = [_c_int]
     lib.fa_status_string.restype = ctypes.c_char_p
@@ -141,6 +147,12 @@ def fa_debug_wait_timeout(timeout_ms: int, stream=None):
     """Test hook: a bounded device wait that runs out after timeout_ms and
     records FA_ERR_DEVICE_TIMEOUT (see the C header)."""
     _check(library().fa_debug_wait_timeout(int(timeout_ms), _stream(stream)), "fa_debug_wait_timeout")
+
+
+def fa_debug_last_kernel() -> int:
+    """Test hook: the partial kernel (FA_KID_*) that this thread's last forward
+    call enqueued (see the C header)."""
+    return int(library().fa_debug_last_kernel())
 
 
 def fa_get_device_error(clear: bool = False) -> int:

@@ -34,6 +34,10 @@ int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The partial kernel the calling thread's last forward call launched
+// (fa_kernel_id), for fa_debug_last_kernel.
+thread_local int t_last_kernel = FA_KID_NONE;
+
 int current_device(int* dev) {
   return cudaGetDevice(dev) == cudaSuccess && *dev >= 0 && *dev < kMaxDevices ? FA_OK : FA_ERR_CUDA;
 }
@@ -285,6 +289,8 @@ int fa_get_device_error(int clear) {
   return v;
 }
 
+int fa_debug_last_kernel(void) { return t_last_kernel; }
+
 int fa_debug_wait_timeout(unsigned int timeout_ms, void* stream) {
   if (timeout_ms < 1 || timeout_ms > 10000) return FA_ERR_INVALID_ARG;
   int* err = nullptr;
@@ -324,6 +330,7 @@ int fwd_impl(const void* q, const void* k, const void* v, const int* cu_seqlens_
              const float* descale_v, int flags, void* stream, const int* block_table,
              const int* seqlens_k, int max_pages, int page_size) {
   const bool paged = page_size > 0;
+  t_last_kernel = FA_KID_NONE;
   // ---- argument validation (synchronous, before any launch)
   if (batch < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0) return FA_ERR_INVALID_ARG;
   if (h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || h_q / h_kv > 128) return FA_ERR_INVALID_ARG;
@@ -436,6 +443,7 @@ int fwd_impl(const void* q, const void* k, const void* v, const int* cu_seqlens_
     st = make_tmap_3d(&tmV, v, in_dtype, d_v, h_kv, total_k, box_keys);
     if (st != FA_OK) return st;
     cudaError_t e;
+    int launched = FA_KID_NONE;
     if (use_umma2) {
       const int qpt = 128 / p.group;
       p.tile_rows = 2 * qpt * p.group;
@@ -466,10 +474,12 @@ int fwd_impl(const void* q, const void* k, const void* v, const int* cu_seqlens_
         if (cudaMemsetAsync(p.sched, 0, sizeof(int), s) != cudaSuccess) return FA_ERR_CUDA;
         e = in_dtype == kFP16 ? launch_umma2p_fp16(d_qk, d_v, p, tmQ, tmK, tmV, grid, s)
                               : launch_umma2p_bf16(d_qk, d_v, p, tmQ, tmK, tmV, grid, s);
+        launched = FA_KID_UMMA2_PERSISTENT;
       } else {
         dim3 grid((unsigned)ceil_div(max_seqlen_q, 2 * qpt), (unsigned)(batch * h_kv), (unsigned)ns);
         e = in_dtype == kFP16 ? launch_umma2_fp16(d_qk, d_v, p, tmQ, tmK, tmV, grid, s)
                               : launch_umma2_bf16(d_qk, d_v, p, tmQ, tmK, tmV, grid, s);
+        launched = FA_KID_UMMA2;
       }
     } else if (use_umma) {
       const int qpt = 128 / p.group;
@@ -479,6 +489,7 @@ int fwd_impl(const void* q, const void* k, const void* v, const int* cu_seqlens_
       if (st != FA_OK) return st;
       dim3 grid((unsigned)ceil_div(max_seqlen_q, qpt), (unsigned)(batch * h_kv), (unsigned)ns);
       e = launch_umma(in_dtype, d_qk, d_v, p, tmQ, tmK, tmV, grid, s);
+      launched = FA_KID_UMMA;
     } else {
       int rt = 1;
       while (rt < rows && rt < rt_max) rt *= 2;
@@ -488,8 +499,10 @@ int fwd_impl(const void* q, const void* k, const void* v, const int* cu_seqlens_
       // different lengths to balance; one sequence keeps the grid order.
       const bool ordered = batch > 1 && batch <= kMaxRankedSeqs;
       e = launch_simt(in_dtype, d_qk, d_v, rt, ordered, p, tmK, tmV, grid, s);
+      launched = FA_KID_SIMT;
     }
     if (e != cudaSuccess) return FA_ERR_CUDA;
+    t_last_kernel = launched;
   }
   if (run_combine && ns > 1) {
     cudaError_t e;

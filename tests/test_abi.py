@@ -124,10 +124,12 @@ def _call_ex(fa, **kw):
 ])
 def test_argument_errors_are_synchronous(fa, kw, status):
     assert _call_ex(fa, **kw) == status
+    assert fa.fa_debug_last_kernel() == fa.FA_KID_NONE  # nothing enqueued
 
 
 def test_empty_problem_is_a_noop(fa):
     assert _call_ex(fa, batch=0) == 0
+    assert fa.fa_debug_last_kernel() == fa.FA_KID_NONE
     assert _call_ex(fa, max_seqlen_q=0) == 0
     assert _call_ex(fa, total_q=0) == 0
 

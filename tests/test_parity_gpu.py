@@ -248,6 +248,41 @@ def test_persistent_prefill_two_streams_own_workspaces():
     assert fa.fa_get_device_error(clear=True) == 0
 
 
+def test_auto_kernel_choice():
+    """AUTO's choice for each rule of the header, as fa_debug_last_kernel
+    reports it: few rows per KV head run on the CUDA cores; up to 128 rows,
+    e4m3 and head dim 256 on the one-tile tcgen05 kernel; more rows (16-bit,
+    d <= 128) on the persistent two-tile kernel when there is one split, a
+    workspace and a 32-byte aligned O, else on the non-persistent one."""
+    last = fa.fa_debug_last_kernel
+    run_gpu(workload("tiny_decode"), num_splits=4)
+    assert last() == fa.FA_KID_SIMT
+    run_gpu(make_inputs([1, 1], [300, 500], 16, 2, 128, 128, "bf16", seed=50))  # 8 rows per KV head
+    assert last() == fa.FA_KID_UMMA
+    run_gpu(workload("fp8_prefix", kv=1024))
+    assert last() == fa.FA_KID_UMMA
+    run_gpu(make_inputs([300], [300], 2, 2, 256, 256, "bf16", seed=51), num_splits=1)
+    assert last() == fa.FA_KID_UMMA
+    lens = [700, 300]
+    inp = _quarter_v(make_inputs(lens, lens, 4, 2, 128, 128, "bf16", seed=52))
+    for causal in (False, True):
+        run_gpu(inp, causal=causal, num_splits=1)
+        assert last() == fa.FA_KID_UMMA2_PERSISTENT
+    run_gpu(inp, num_splits=1, out_offset=16)
+    assert last() == fa.FA_KID_UMMA2
+    run_gpu(inp, num_splits=2)
+    assert last() == fa.FA_KID_UMMA2
+    run_gpu(inp, num_splits=1, flags=fa.FA_KERNEL_UMMA2)
+    assert last() == fa.FA_KID_UMMA2
+    q, k, v, cq, ck, out, lse, ws = _prefill_buffers(inp, torch.device("cuda:0"))
+    fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, inp.max_seqlen_q, out, lse, None, num_splits=1)
+    torch.cuda.synchronize()
+    assert last() == fa.FA_KID_UMMA2  # no workspace: no tile counter
+    o_ref, l_ref = reference(inp, 0.0, False)
+    assert_close(inp, out.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref)
+    assert fa.fa_get_device_error(clear=True) == 0
+
+
 def test_partial_then_combine_equals_single_call():
     inp = workload("long_decode", kv=3000, h=4)
     a_out, a_lse = run_gpu(inp, num_splits=5)

@@ -131,8 +131,10 @@ typedef enum {
  *                 head dim 256, and the two-tile tcgen05 kernel beyond 128
  *                 rows (16-bit, head dim <= 128; its persistent form for one
  *                 split over packed K/V with a workspace and a 32-byte
- *                 aligned out, at most 128 sequences).  FA_KERNEL_UMMA2
- *                 always runs the non-persistent two-tile kernel.
+ *                 aligned out, at most 128 sequences and batch *
+ *                 ceil(max_seqlen_q / (256 / group)) <= 4096 query pairs).
+ *                 FA_KERNEL_UMMA2 always runs the non-persistent two-tile
+ *                 kernel.
  *  stream         cudaStream_t.
  * Returns FA_OK or a negative fa_status.
  */

@@ -16,8 +16,9 @@ namespace fa {
 constexpr int kBlockN = 128;    // keys per split block
 constexpr int kMaxSplits = 128;
 // Tile list of the persistent two-tile kernel: (sequence, 256-row query pair)
-// units held in shared memory, 7 bits of sequence and 9 of pair each.
-constexpr int kMaxUnits = 640;
+// units held in shared memory, 7 bits of sequence and 9 of pair each.  The
+// host bounds the units by batch * pairs of the longest sequence.
+constexpr int kMaxUnits = 4096;
 constexpr int kMaxUnitPairs = 512;
 // Slots of the ring through which its producer hands each claimed tile to the
 // MMA and softmax roles.

@@ -284,15 +284,15 @@ def test_auto_kernel_choice():
 
 
 @pytest.mark.parametrize("lens,persistent", [
-    ([257] * 128, True), ([257] * 129, False),
-    ([2048] * 80, True), ([2048] * 81, False)])
+    ([40] * 128, True), ([40] * 129, False),
+    ([1024] + [40] * 127, True), ([1056] + [40] * 127, False)])
 def test_persistent_capacity(lens, persistent):
-    """The persistent kernel's tile list holds 128 sequences and 640
-    (sequence, 256-query pair) units; the host, which cannot read cu_seqlens,
-    bounds the units by batch x ceil(max_seqlen_q / 256).  128 sequences, or
-    80 x 8 = 640 units, fit; 129 sequences, or 81 x 8 = 648 units, run the
-    non-persistent kernel instead.  Results are correct either way."""
-    inp = _quarter_v(make_inputs(lens, lens, 2, 2, 64, 64, "bf16", seed=53))
+    """The persistent kernel's tile list holds 128 sequences and 4096
+    (sequence, query pair) units; the host, which cannot read cu_seqlens,
+    bounds the units by batch x pairs of the longest sequence.  With GQA 8:1 a
+    pair is 32 queries: 128 x 32 = 4096 units fit, 128 x 33 = 4224 and 129
+    sequences run the non-persistent kernel.  Results are correct either way."""
+    inp = _quarter_v(make_inputs(lens, lens, 16, 2, 64, 64, "bf16", seed=53))
     out, lse = run_gpu(inp, causal=True, num_splits=1)
     assert fa.fa_debug_last_kernel() == (fa.FA_KID_UMMA2_PERSISTENT if persistent else fa.FA_KID_UMMA2)
     o_ref, l_ref = reference(inp, 0.0, True)

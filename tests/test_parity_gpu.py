@@ -283,6 +283,31 @@ def test_auto_kernel_choice():
     assert fa.fa_get_device_error(clear=True) == 0
 
 
+@pytest.mark.parametrize("seed", range(60, 68))
+def test_persistent_prefill_random_shapes(seed):
+    """Random batches on the persistent kernel: 1-12 sequences with query and
+    key lengths drawn independently from 0-900 (the first at least 300, so
+    there are more than 128 rows per KV head), GQA 1:1 to 8:1 with one or two
+    KV heads, head dim 64 or 128, bf16 or fp16, no mask, causal or a random
+    window; guard rows after the packed queries stay untouched."""
+    rng = np.random.default_rng(seed)
+    batch = int(rng.integers(1, 13))
+    lq = [int(x) for x in rng.integers(0, 900, size=batch)]
+    lk = [int(x) for x in rng.integers(0, 900, size=batch)]
+    lq[0] = max(lq[0], 300)
+    group, h_kv = int(rng.choice([1, 2, 4, 8])), int(rng.choice([1, 2]))
+    d = int(rng.choice([64, 128]))
+    dtype = str(rng.choice(["bf16", "fp16"]))
+    mask = str(rng.choice(["none", "causal", "window"]))
+    causal = mask == "causal"
+    wl = int(rng.integers(0, 300)) if mask == "window" else -1
+    inp = _quarter_v(make_inputs(lq, lk, group * h_kv, h_kv, d, d, dtype, seed=seed))
+    out, lse = run_gpu(inp, causal=causal, window_left=wl, num_splits=1, guard_rows=1)
+    assert fa.fa_debug_last_kernel() == fa.FA_KID_UMMA2_PERSISTENT
+    o_ref, l_ref = reference(inp, 0.0, causal, wl)
+    assert_close(inp, out, lse, o_ref, l_ref)
+
+
 @pytest.mark.parametrize("lens,persistent", [
     ([40] * 128, True), ([40] * 129, False),
     ([1024] + [40] * 127, True), ([1056] + [40] * 127, False)])

@@ -46,6 +46,10 @@ CASES = {
     "causal_prefix_3_splits": (
         lambda: make_inputs([3, 40, 1], [200, 300, 64], 8, 2, 128, 128, "bf16", seed=12),
         dict(num_splits=3, causal=True)),
+    # one split: the persistent prefill kernel, its tile counter in the array
+    "causal_prefill_persistent": (
+        lambda: make_inputs([700, 300, 520], [700, 300, 520], 4, 2, 128, 128, "bf16", seed=13),
+        dict(num_splits=1, causal=True, kernel=fa.FA_KID_UMMA2_PERSISTENT)),
 }
 
 
@@ -72,6 +76,8 @@ def test_noalloc_matches_caller_workspace_path(name):
         out, lse = _outputs(inp, q)
         fa.fa_fwd_splitkv_noalloc(q, k, v, cq, ck, inp.max_seqlen_q, out, lse,
                                   causal=kw.get("causal", False), num_splits=ns)
+        if "kernel" in kw:
+            assert fa.fa_debug_last_kernel() == kw["kernel"]
         torch.cuda.synchronize()
         assert fa.fa_get_device_error(clear=True) == 0
         o = out.float().cpu().numpy()

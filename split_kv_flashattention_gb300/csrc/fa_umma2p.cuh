@@ -301,9 +301,10 @@ __global__ void __launch_bounds__(384, 1)
           ++issued_v;
           return true;
         };
-        // Q and the first K/V block of a tile into L2, a tile ahead: the
-        // tile's own Q load can only start once the previous tile's last S
-        // MMAs have read the old Q, and then finds it in L2.
+        // Q and the first K/V block of a claimed tile into L2 while the
+        // current tile's last blocks run: the tile's own Q load can only start
+        // once the current tile's last S MMAs have read the old Q, and then
+        // finds it in L2.
         auto prefetch_tile = [&](const PTile& T) {
           const int ntiles = T.nq_b > 0 ? 2 : 1;
           for (int t = 0; t < ntiles; ++t)
@@ -318,8 +319,8 @@ __global__ void __launch_bounds__(384, 1)
             tma_prefetch_l2_3d(&tmV, pv * C::PANEL_ELEMS, T.kh, T.sq.k0 + T.kb0);
         };
         // Every CTA's first tile is its own index; each later one is claimed
-        // from the ticket counter when the tile before it starts, so the
-        // tiles (longest first) go to whichever CTA is free first.
+        // from the ticket counter once the tile before it has issued all its
+        // loads, so the tiles (longest first) go to whichever CTA is free.
         int claimed = (int)blockIdx.x < n_tiles ? (int)blockIdx.x : -1;
         for (int k = 0; ok; ++k) {
           const int r = claimed;

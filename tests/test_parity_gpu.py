@@ -308,6 +308,21 @@ def test_persistent_prefill_random_shapes(seed):
     assert_close(inp, out, lse, o_ref, l_ref)
 
 
+@pytest.mark.parametrize("group", [16, 32, 128])
+@pytest.mark.parametrize("mask", ["none", "causal", "window"])
+def test_persistent_prefill_large_groups(group, mask):
+    """GQA groups of 16 to 128 query heads per KV head: a 128-row tile then
+    holds 8, 4 or 1 queries, and a pair 16, 8 or 2."""
+    lens_q, lens_k = [150, 37, 0, 90], [150, 60, 25, 90]
+    inp = _quarter_v(make_inputs(lens_q, lens_k, group, 1, 64, 64, "bf16", seed=54 + group))
+    causal = mask == "causal"
+    wl = 40 if mask == "window" else -1
+    out, lse = run_gpu(inp, causal=causal, window_left=wl, num_splits=1, guard_rows=1)
+    assert fa.fa_debug_last_kernel() == fa.FA_KID_UMMA2_PERSISTENT
+    o_ref, l_ref = reference(inp, 0.0, causal, wl)
+    assert_close(inp, out, lse, o_ref, l_ref)
+
+
 @pytest.mark.parametrize("lens,persistent", [
     ([40] * 128, True), ([40] * 129, False),
     ([1024] + [40] * 127, True), ([1056] + [40] * 127, False)])

@@ -71,6 +71,11 @@ WORKLOADS = {
                               "H_kv=8, D=128, K lengths U[1024,32768] seed 0, 64-key pages, bf16"),
     "prefill_gqa_causal": dict(name="prefill", kw={"h_kv": 4}, causal=True, kind="tensor",
                                desc="varlen prefill: 16384 tokens, H_q=16, H_kv=4, D=128, bf16, causal"),
+    "prefill_fp16": dict(name="prefill", kw={"h_kv": 16, "dtype": "fp16"}, causal=False, kind="tensor",
+                         desc="varlen prefill: 16384 tokens, H_q=H_kv=16, D=128, fp16, no mask"),
+    "prefill_causal_fp16": dict(name="prefill", kw={"h_kv": 16, "dtype": "fp16"}, causal=True,
+                                kind="tensor",
+                                desc="varlen prefill: 16384 tokens, H_q=H_kv=16, D=128, fp16, causal"),
 }
 
 
@@ -576,8 +581,9 @@ def main():
         if kind == "tensor":
             peak, peak_sus, src = measured_tensor_peak()
             achieved = work_flops / (partial_ms * 1e-3) / 1e12
+            same_rate = "" if inp.dtype == "bf16" else f"; {inp.dtype} dense at the bf16 nominal rate (1:1)"
             roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "peak_source": src + " bf16 dense (burst)",
+                    "frac": achieved / peak, "peak_source": src + " bf16 dense (burst)" + same_rate,
                     "traffic": profiled_traffic(kern_tag, args.workload),
                     "kernel": f"{kern_tag} partial kernel", "partial_ms": partial_ms,
                     "timing": "K partial-only launches, CUDA events",

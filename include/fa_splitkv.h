@@ -125,10 +125,11 @@ typedef enum {
  *  descale_q/k/v  device float32 scalars, required for FA_E4M3 inputs
  *                 (per-tensor dequantisation factors), ignored otherwise.
  *  flags          FA_KERNEL_* selection, optionally OR FA_RUN_*_ONLY.  AUTO
- *                 picks the CUDA-core kernel for up to 4 rows (queries x
- *                 group) per KV head (2 for e4m3 with d_qk=192), the
- *                 one-tile tcgen05 kernel up to 128 rows, for e4m3 and for
- *                 head dim 256, and the two-tile tcgen05 kernel beyond 128
+ *                 picks the CUDA-core kernel for up to 2 rows (queries x
+ *                 group) per KV head (up to 4 with head dim 64), the
+ *                 one-tile tcgen05 kernel above that up to 128 rows and, for
+ *                 e4m3 and head dim 256, beyond; and the two-tile tcgen05
+ *                 kernel beyond 128
  *                 rows (16-bit, head dim <= 128; its persistent form for one
  *                 split over packed K/V with a workspace and a 32-byte
  *                 aligned out, at most 128 sequences and batch *

@@ -164,6 +164,16 @@ int simt_max_rows(int dtype, int d_qk, int d_v) {
   return 4;
 }
 
+// The most rows per KV head AUTO gives the CUDA-core kernel.  Measured on
+// varlen and long decode: from 3 rows on (d = 128, 16-bit and e4m3) the
+// one-tile tensor-core kernel streams K/V faster (GQA-4 batch: 6.87 against
+// 6.21 TB/s), with 1 or 2 rows the CUDA-core kernel does; with d = 64 it
+// stays ahead up to its 4-row limit.
+int simt_auto_rows(int dtype, int d_qk, int d_v) {
+  const int m = simt_max_rows(dtype, d_qk, d_v);
+  return d_qk == 64 ? m : (m < 2 ? m : 2);
+}
+
 cudaError_t launch_simt(int dtype, int d_qk, int d_v, int rt, bool ordered, const FwdParams& p,
                         const CUtensorMap& tmK, const CUtensorMap& tmV, dim3 grid,
                         cudaStream_t stream) {
@@ -426,7 +436,7 @@ int fwd_impl(const void* q, const void* k, const void* v, const int* cu_seqlens_
   // cores; more rows form a dense contraction for the tensor cores.
   const int rows = max_seqlen_q * p.group;
   const int rt_max = simt_max_rows(in_dtype, d_qk, d_v);
-  const bool auto_tc = kernel_sel == FA_KERNEL_AUTO && rows > rt_max;
+  const bool auto_tc = kernel_sel == FA_KERNEL_AUTO && rows > simt_auto_rows(in_dtype, d_qk, d_v);
   // More than one 128-row tile per KV head with 16-bit inputs: two tiles per
   // CTA share each K/V block and overlap their softmax with the other tile's
   // MMAs.  Otherwise one tile per CTA.

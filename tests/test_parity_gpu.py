@@ -250,13 +250,20 @@ def test_persistent_prefill_two_streams_own_workspaces():
 
 def test_auto_kernel_choice():
     """AUTO's choice for each rule of the header, as fa_debug_last_kernel
-    reports it: few rows per KV head run on the CUDA cores; up to 128 rows,
-    e4m3 and head dim 256 on the one-tile tcgen05 kernel; more rows (16-bit,
-    d <= 128) on the persistent two-tile kernel when there is one split, a
-    workspace and a 32-byte aligned O, else on the non-persistent one."""
+    reports it: up to 2 rows per KV head (4 with head dim 64) run on the CUDA
+    cores; up to 128 rows, e4m3 and head dim 256 on the one-tile tcgen05
+    kernel; more rows (16-bit, d <= 128) on the persistent two-tile kernel
+    when there is one split, a workspace and a 32-byte aligned O, else on the
+    non-persistent one."""
     last = fa.fa_debug_last_kernel
     run_gpu(workload("tiny_decode"), num_splits=4)
     assert last() == fa.FA_KID_SIMT
+    run_gpu(make_inputs([1, 1], [300, 500], 4, 2, 128, 128, "bf16", seed=55))  # 2 rows per KV head
+    assert last() == fa.FA_KID_SIMT
+    run_gpu(make_inputs([1, 1], [300, 500], 8, 2, 64, 64, "bf16", seed=56))  # 4 rows, head dim 64
+    assert last() == fa.FA_KID_SIMT
+    run_gpu(make_inputs([1, 1], [300, 500], 8, 2, 128, 128, "bf16", seed=57))  # 4 rows
+    assert last() == fa.FA_KID_UMMA
     run_gpu(make_inputs([1, 1], [300, 500], 16, 2, 128, 128, "bf16", seed=50))  # 8 rows per KV head
     assert last() == fa.FA_KID_UMMA
     run_gpu(workload("fp8_prefix", kv=1024))

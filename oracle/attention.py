@@ -18,7 +18,7 @@ re-association):
   cu_seqlens[b+1]-1.  dq, dk, dv are per-tensor FP8 descales ([AITER]
   description: FP8 FMHA); they are 1 for 16-bit inputs.
 
-Readings where the pages are silent (listed again in the design doc):
+Readings where the pages are silent:
 
 * LSE is the natural log and includes the softmax scale.
 * LSE is laid out [h_q, total_q].

@@ -16,7 +16,7 @@ Recipe (same for every workload):
   stored codes e4m3(x / descale) (round to nearest even); the descale is a
   float32 scalar.  Quantisation is input preparation, not part of the path.
 
-Named workloads mirror the shapes the pages measure (see DESIGN.md).
+Named workloads mirror the shapes the pages measure.
 """
 
 from __future__ import annotations
@@ -116,7 +116,7 @@ def make_inputs(lens_q, lens_k, h_q: int, h_kv: int, d_qk: int, d_v: int,
 
 
 # ----------------------------------------------------------------------------
-# Named workloads (shapes from the pages; see the design doc for the mapping).
+# Named workloads (shapes from the pages).
 
 def gqa_decode_lengths(seed: int = 0, batch: int = 32):
     """Per-sequence key lengths uniform in [1024, 32768] from the seed."""

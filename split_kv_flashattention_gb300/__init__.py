@@ -109,6 +109,70 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _tensor(t, name, shape=None, dtypes=None, optional=False):
+    """Checks one argument before its pointer goes to the library, which only
+    sees addresses: a strided view, a wrong dtype or shape, or host memory
+    would otherwise be read as the packed device layout."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}; expected one of {sorted(map(str, dtypes))}")
+    if shape is not None and t.shape != shape:
+        raise ValueError(f"{name} has shape {tuple(t.shape)}; expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _on_device(ref, **tensors):
+    """Every given tensor must live on the CUDA device of `ref`."""
+    if not ref.is_cuda:
+        raise ValueError("inputs must be CUDA tensors (device memory), got a "
+                         f"{ref.device.type} tensor")
+    dev = ref.get_device()
+    for name, t in tensors.items():
+        if t is not None and t.get_device() != dev:
+            raise ValueError(f"{name} is on {t.device}, the inputs on {ref.device}")
+
+
+_INPUT_DTYPES = tuple(DTYPE_CODES)
+_I32 = (torch.int32,)
+_F32 = (torch.float32,)
+
+
+def _check_forward_args(q, k, v, cu_seqlens_q, seqlens_k_name, seqlens_k, out, lse, workspace,
+                        descales, kv_ndim=3):
+    """Shapes, dtypes, contiguity and device of a forward call's tensors."""
+    _tensor(q, "q", dtypes=_INPUT_DTYPES)
+    _tensor(k, "k", dtypes=(q.dtype,))
+    _tensor(v, "v", dtypes=(q.dtype,))
+    if q.dim() != 3 or k.dim() != kv_ndim or v.dim() != kv_ndim:
+        raise ValueError(f"q must be 3-D and k, v {kv_ndim}-D; got {q.dim()}, {k.dim()}, {v.dim()}")
+    if tuple(k.shape[:-1]) != tuple(v.shape[:-1]):
+        raise ValueError(f"k {tuple(k.shape)} and v {tuple(v.shape)} differ before the head dim")
+    if k.shape[-1] != q.shape[2]:
+        raise ValueError(f"q and k head dims differ ({q.shape[2]} vs {k.shape[-1]})")
+    _tensor(cu_seqlens_q, "cu_seqlens_q", dtypes=_I32)
+    if cu_seqlens_q.dim() != 1 or cu_seqlens_q.numel() < 1:
+        raise ValueError("cu_seqlens_q must be 1-D with batch+1 entries")
+    batch = cu_seqlens_q.numel() - 1
+    n_k = batch + 1 if seqlens_k_name == "cu_seqlens_k" else batch
+    _tensor(seqlens_k, seqlens_k_name, shape=(n_k,), dtypes=_I32)
+    total_q, h_q = q.shape[0], q.shape[1]
+    _tensor(out, "out", shape=(total_q, h_q, v.shape[-1]), dtypes=_INPUT_DTYPES)
+    _tensor(lse, "lse", shape=(h_q, total_q), dtypes=_F32, optional=True)
+    _tensor(workspace, "workspace", optional=True)
+    for name, d in descales.items():
+        _tensor(d, name, dtypes=_F32, optional=True)
+        if d is not None and d.numel() < 1:
+            raise ValueError(f"{name} must hold one float32 value")
+    _on_device(q, k=k, v=v, cu_seqlens_q=cu_seqlens_q, **{seqlens_k_name: seqlens_k}, out=out,
+               lse=lse, workspace=workspace, **descales)
+
+
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -162,6 +226,9 @@ def fa_get_device_error(clear: bool = False) -> int:
 def fa_debug_split_ranges(cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal: bool,
                           window_left: int, num_splits: int, tile_queries: int, stream=None):
     """Device-computed key ranges, int32 [m_blocks, batch, num_splits, 2]."""
+    _tensor(cu_seqlens_q, "cu_seqlens_q", dtypes=_I32)
+    _tensor(cu_seqlens_k, "cu_seqlens_k", shape=tuple(cu_seqlens_q.shape), dtypes=_I32)
+    _on_device(cu_seqlens_q, cu_seqlens_k=cu_seqlens_k)
     batch = cu_seqlens_q.numel() - 1
     m_blocks = -(-max_seqlen_q // tile_queries)
     out = torch.full((m_blocks, batch, num_splits, 2), -1, dtype=torch.int32,
@@ -180,6 +247,8 @@ def fa_fwd_splitkv_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, ou
                       stream=None):
     """Calls fa_fwd_splitkv_ex on torch CUDA tensors (shapes read from them).
     flags: FA_KERNEL_* optionally OR-ed with FA_RUN_PARTIAL_ONLY/COMBINE_ONLY."""
+    _check_forward_args(q, k, v, cu_seqlens_q, "cu_seqlens_k", cu_seqlens_k, out, lse, workspace,
+                        dict(descale_q=descale_q, descale_k=descale_k, descale_v=descale_v))
     total_q, h_q, d_qk = q.shape
     total_k, h_kv, _ = k.shape
     d_v = v.shape[2]
@@ -204,6 +273,8 @@ def fa_fwd_splitkv_noalloc(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: in
     workspace is the library's fixed device array of NOALLOC_SCRATCH_BYTES;
     larger problems raise FaError(FA_ERR_WORKSPACE).  Calls that overlap on
     the GPU share that array and must be serialised by the caller."""
+    _check_forward_args(q, k, v, cu_seqlens_q, "cu_seqlens_k", cu_seqlens_k, out, lse, None,
+                        dict(descale_q=descale_q, descale_k=descale_k, descale_v=descale_v))
     total_q, h_q, d_qk = q.shape
     total_k, h_kv, _ = k.shape
     st = library().fa_fwd_splitkv_noalloc(
@@ -222,6 +293,14 @@ def fa_fwd_splitkv_paged(q, k_cache, v_cache, cu_seqlens_q, seqlens_k, block_tab
                          flags: int = FA_KERNEL_AUTO, stream=None):
     """Calls fa_fwd_splitkv_paged: K/V caches [num_pages, page_size, h_kv, d],
     block_table int32 [batch, max_pages], seqlens_k int32 [batch]."""
+    _tensor(block_table, "block_table", dtypes=_I32)
+    if block_table.dim() != 2 or block_table.shape[0] != cu_seqlens_q.numel() - 1:
+        raise ValueError(f"block_table must be [batch, max_pages]; got {tuple(block_table.shape)}")
+    _check_forward_args(q, k_cache, v_cache, cu_seqlens_q, "seqlens_k", seqlens_k, out, lse,
+                        workspace,
+                        dict(descale_q=descale_q, descale_k=descale_k, descale_v=descale_v),
+                        kv_ndim=4)
+    _on_device(q, block_table=block_table)
     total_q, h_q, d_qk = q.shape
     num_pages, page_size, h_kv, _ = k_cache.shape
     d_v = v_cache.shape[3]
@@ -241,6 +320,10 @@ def fa_fwd_splitkv(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, out, 
                    workspace=None, scale: float = 0.0, causal: bool = False,
                    window_left: int = -1, num_splits: int = 0, stream=None):
     """Calls the bf16 shorthand entry point fa_fwd_splitkv."""
+    _check_forward_args(q, k, v, cu_seqlens_q, "cu_seqlens_k", cu_seqlens_k, out, lse, workspace,
+                        {})
+    if q.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+        raise ValueError("fa_fwd_splitkv takes bf16 q, k, v and out; use fa_fwd_splitkv_ex")
     total_q, h_q, d_qk = q.shape
     total_k, h_kv, _ = k.shape
     st = library().fa_fwd_splitkv(

@@ -199,8 +199,10 @@ FA_API int fa_fwd_splitkv(const void* q, const void* k, const void* v, const int
  * with that device current (make it before any stream capture).  All calls
  * on a device share the one array: calls that may overlap on the GPU (other
  * streams, other host threads) race on it and must be serialised by the
- * caller.  The array keeps the last call's contents; nothing in it needs
- * clearing because every partial a call reads was written by that call.
+ * caller.  The array keeps the last call's contents.  Every partial a call
+ * reads was written by that call, and the one word that must start at zero
+ * (the persistent prefill kernel's tile counter) is zeroed in stream order by
+ * each call before its launch.
  */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20) /* 8 MiB */
 FA_API int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v,

@@ -26,9 +26,10 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr size_t kScratchFloats = FA_NOALLOC_SCRATCH_BYTES / sizeof(float);
 
-// Shared by every call on a device.  Holds whatever the last call left;
-// the split kernels write every partial they later read, so nothing needs
-// clearing between calls.
+// Shared by every call on a device.  Holds whatever the last call left.
+// The split kernels write every partial they later read, and the one word
+// that must start at zero (the persistent prefill kernel's tile counter in
+// the first bytes) is zeroed in stream order by each call before its launch.
 static __device__ __align__(256) float g_noalloc_scratch[kScratchFloats];
 
 std::mutex g_mu;

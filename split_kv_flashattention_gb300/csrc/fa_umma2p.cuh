@@ -105,7 +105,8 @@ __device__ __forceinline__ void decode_ptile(const FwdParams& p, const uint16_t*
   t.nblk = t.k1 > t.k0 ? (t.k1 - t.kb0 + kBlockN - 1) / kBlockN : 0;
 }
 
-template <int DT, int DQK, int DV, int KS, int VS>
+// MASKED: instantiated for calls with a causal or window mask.
+template <int DT, int DQK, int DV, int KS, int VS, bool MASKED>
 __global__ void __launch_bounds__(384, 1)
     umma2p_splitkv_kernel(const __grid_constant__ FwdParams p,
                           const __grid_constant__ CUtensorMap tmQ,
@@ -569,10 +570,24 @@ __global__ void __launch_bounds__(384, 1)
           float s[128];
           tmem_ld128(s_addr, reinterpret_cast<uint32_t*>(s));
           if (__any_sync(0xffffffffu, !(kb >= lo && kb + kBlockN <= hi))) {
+            // Under a causal mask most cut blocks are cut by the right bound
+            // alone: one compare per key.  The unmasked instantiation only
+            // meets sequence tails and keeps the general form alone.
+            bool cut = false;
+            if constexpr (MASKED) {
+              if (__all_sync(0xffffffffu, kb >= lo)) {
+                const int c_hi = hi - kb;
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-              const int key = kb + c;
-              s[c] = (key >= lo && key < hi) ? s[c] : -CUDART_INF_F;
+                for (int c = 0; c < 128; ++c) s[c] = c < c_hi ? s[c] : -CUDART_INF_F;
+                cut = true;
+              }
+            }
+            if (!cut) {
+#pragma unroll
+              for (int c = 0; c < 128; ++c) {
+                const int key = kb + c;
+                s[c] = (key >= lo && key < hi) ? s[c] : -CUDART_INF_F;
+              }
             }
           }
           float mx[8];

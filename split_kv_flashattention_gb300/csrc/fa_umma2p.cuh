@@ -568,64 +568,83 @@ __global__ void __launch_bounds__(384, 1)
         if (warp_active) {
           const int kb = T.kb0 + j * kBlockN;
           float s[128];
-          tmem_ld128(s_addr, reinterpret_cast<uint32_t*>(s));
-          if (__any_sync(0xffffffffu, !(kb >= lo && kb + kBlockN <= hi))) {
-            // Under a causal mask most cut blocks are cut by the right bound
-            // alone: one compare per key.  The unmasked instantiation only
-            // meets sequence tails and keeps the general form alone.
-            bool cut = false;
-            if constexpr (MASKED) {
-              if (__all_sync(0xffffffffu, kb >= lo)) {
-                const int c_hi = hi - kb;
+          float m_new = m_run, alpha = 1.f, rsum = 0.f;
+          // Once every row of the warp has a running max, the exponentials
+          // are first taken against it without the block max.  A row sum of
+          // at most 2^8 means that no probability exceeds 2^8, which the lazy
+          // rescale allows without moving the max, so the block max was not
+          // needed.  Otherwise (rare after a tile's first block) the scores
+          // are read again and the block takes the second pass with its max.
+          // Both give the same result bit for bit.
+          bool with_max = !__all_sync(0xffffffffu, m_run != -CUDART_INF_F);
+#pragma unroll 1
+          for (;;) {
+            tmem_ld128(s_addr, reinterpret_cast<uint32_t*>(s));
+            if (__any_sync(0xffffffffu, !(kb >= lo && kb + kBlockN <= hi))) {
+              // Under a causal mask most cut blocks are cut by the right bound
+              // alone: one compare per key.  The unmasked instantiation only
+              // meets sequence tails and keeps the general form alone.
+              bool cut = false;
+              if constexpr (MASKED) {
+                if (__all_sync(0xffffffffu, kb >= lo)) {
+                  const int c_hi = hi - kb;
 #pragma unroll
-                for (int c = 0; c < 128; ++c) s[c] = c < c_hi ? s[c] : -CUDART_INF_F;
-                cut = true;
+                  for (int c = 0; c < 128; ++c) s[c] = c < c_hi ? s[c] : -CUDART_INF_F;
+                  cut = true;
+                }
+              }
+              if (!cut) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                  const int key = kb + c;
+                  s[c] = (key >= lo && key < hi) ? s[c] : -CUDART_INF_F;
+                }
               }
             }
-            if (!cut) {
+            float m_use = m_run;
+            if (with_max) {
+              float mx[8];
 #pragma unroll
-              for (int c = 0; c < 128; ++c) {
-                const int key = kb + c;
-                s[c] = (key >= lo && key < hi) ? s[c] : -CUDART_INF_F;
+              for (int u = 0; u < 8; ++u) mx[u] = -CUDART_INF_F;
+#pragma unroll
+              for (int c = 0; c < 128; c += 16)
+#pragma unroll
+                for (int u = 0; u < 8; ++u) mx[u] = fmax3(mx[u], s[c + u], s[c + 8 + u]);
+              const float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+              m_new = (bmax > m_run + 8.f) ? bmax : m_run;  // lazy rescale, 2^8
+              m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
+              alpha = m_run == m_new ? 1.f : fast_exp2(m_run - m_use);
+              const bool rescale = j > 0 && m_run != -CUDART_INF_F && alpha != 1.f;
+              if (__any_sync(0xffffffffu, rescale)) {
+                // O holds block j-1's result: the S(j) commit covered PV(j-1).
+#pragma unroll
+                for (int c = 0; c < DV / 32; ++c) {
+                  uint32_t o[32];
+                  tmem_ld32(o_addr + 32 * c, o);
+#pragma unroll
+                  for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+                  tmem_st32(o_addr + 32 * c, o);
+                }
               }
             }
-          }
-          float mx[8];
+            const f32x2 sl2x2 = f2_make(sl2, sl2);
+            const f32x2 noff = f2_make(-m_use, -m_use);
+            f32x2 sm[4];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) mx[u] = -CUDART_INF_F;
+            for (int u = 0; u < 4; ++u) sm[u] = 0ull;
 #pragma unroll
-          for (int c = 0; c < 128; c += 16)
-#pragma unroll
-            for (int u = 0; u < 8; ++u) mx[u] = fmax3(mx[u], s[c + u], s[c + 8 + u]);
-          const float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
-          const float m_new = (bmax > m_run + 8.f) ? bmax : m_run;  // lazy rescale, 2^8
-          const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
-          const float alpha = m_run == m_new ? 1.f : fast_exp2(m_run - m_use);
-          const bool rescale = j > 0 && m_run != -CUDART_INF_F && alpha != 1.f;
-          if (__any_sync(0xffffffffu, rescale)) {
-            // O holds block j-1's result: the S(j) commit covered PV(j-1).
-#pragma unroll
-            for (int c = 0; c < DV / 32; ++c) {
-              uint32_t o[32];
-              tmem_ld32(o_addr + 32 * c, o);
-#pragma unroll
-              for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
-              tmem_st32(o_addr + 32 * c, o);
+            for (int c = 0; c < 128; c += 2) {
+              const float2 x = f2_split(f2_fma(f2_make(s[c], s[c + 1]), sl2x2, noff));
+              const float e0 = fast_exp2(x.x), e1 = fast_exp2(x.y);
+              s[c] = e0;
+              s[c + 1] = e1;
+              sm[(c >> 1) & 3] = f2_add(sm[(c >> 1) & 3], f2_make(e0, e1));
             }
-          }
-          const f32x2 sl2x2 = f2_make(sl2, sl2);
-          const f32x2 noff = f2_make(-m_use, -m_use);
-          f32x2 sm[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) sm[u] = 0ull;
-#pragma unroll
-          for (int c = 0; c < 128; c += 2) {
-            const float2 x = f2_split(f2_fma(f2_make(s[c], s[c + 1]), sl2x2, noff));
-            const float e0 = fast_exp2(x.x), e1 = fast_exp2(x.y);
-            s[c] = e0;
-            s[c + 1] = e1;
-            sm[(c >> 1) & 3] = f2_add(sm[(c >> 1) & 3], f2_make(e0, e1));
+            const float2 r01 = f2_split(f2_add(f2_add(sm[0], sm[1]), f2_add(sm[2], sm[3])));
+            rsum = r01.x + r01.y;
+            if (with_max || !__any_sync(0xffffffffu, !(rsum <= 256.f))) break;
+            with_max = true;
           }
           // P over the first 64 columns of this tile's S buffer (already read)
 #pragma unroll
@@ -636,8 +655,7 @@ __global__ void __launch_bounds__(384, 1)
             tmem_st32(s_addr + 32 * h2, pk);
           }
           tmem_st_wait();
-          const float2 r01 = f2_split(f2_add(f2_add(sm[0], sm[1]), f2_add(sm[2], sm[3])));
-          l_run = l_run * alpha + (r01.x + r01.y);
+          l_run = l_run * alpha + rsum;
           m_run = m_new;
         }
         tc_fence_before();

@@ -379,25 +379,29 @@ __global__ void __launch_bounds__(384, 1)
     } else if (warp == 1) {
       // ---------------------------------------------------------------- MMA
       if (lane == 0) {
+        // The operand descriptors are built once per call; a k-step only
+        // moves the start address (bits 0-13, in 16-byte units), so it adds
+        // to the low word.  This single thread issues every MMA of the CTA
+        // while sharing its scheduler with two softmax warps, so its
+        // instruction count per MMA shows in the tensor pipe's idle time.
         auto issue_s = [&](int t, int kst) {
-          const uint32_t q_addr = sbase + C::OFF_Q + t * C::NPQ * C::PANEL;
-          const uint32_t k_addr = sbase + C::OFF_K + kst * C::K_STAGE;
+          const uint64_t qd = smem_desc_sw128(sbase + C::OFF_Q + t * C::NPQ * C::PANEL, 16, 1024);
+          const uint64_t kd = smem_desc_sw128(sbase + C::OFF_K + kst * C::K_STAGE, 16, 1024);
 #pragma unroll
           for (int ks = 0; ks < C::S_KSTEPS; ++ks) {
             const uint32_t off =
-                (ks / C::KSTEPS_PER_PANEL) * C::PANEL + (ks % C::KSTEPS_PER_PANEL) * 32;
-            tc_mma_f16(tmem + C::tm_s(t), smem_desc_sw128(q_addr + off, 16, 1024),
-                       smem_desc_sw128(k_addr + off, 16, 1024), C::IDESC_S, ks > 0 ? 1u : 0u);
+                ((ks / C::KSTEPS_PER_PANEL) * C::PANEL + (ks % C::KSTEPS_PER_PANEL) * 32) >> 4;
+            tc_mma_f16(tmem + C::tm_s(t), qd + off, kd + off, C::IDESC_S, ks > 0 ? 1u : 0u);
           }
           tc_commit(s_full + 8 * t);
         };
         auto issue_pv = [&](int t, int vst, bool first) {
-          const uint32_t v_addr = sbase + C::OFF_V + vst * C::V_STAGE;
+          const uint64_t vd = smem_desc_sw128(sbase + C::OFF_V + vst * C::V_STAGE, C::PANEL, 1024);
 #pragma unroll
           for (int ks = 0; ks < C::PV_KSTEPS; ++ks)
             tc_mma_f16_ts(tmem + C::tm_o(t), tmem + C::tm_s(t) + ks * 8,
-                          smem_desc_sw128(v_addr + ks * C::UMMA_K * 128, C::PANEL, 1024),
-                          C::IDESC_PV, (!first || ks > 0) ? 1u : 0u);
+                          vd + ((ks * C::UMMA_K * 128) >> 4), C::IDESC_PV,
+                          (!first || ks > 0) ? 1u : 0u);
         };
         // Running counts: Q tiles and K/V blocks consumed, ring entries read;
         // per slot (bit t) the parity of its p_ready waits and O tiles, and

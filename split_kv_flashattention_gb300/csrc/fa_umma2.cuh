@@ -267,23 +267,27 @@ __global__ void __launch_bounds__(384, 1)
     // ------------------------------------------------------------------ MMA
     if (lane == 0 && nblk > 0) {
       const int ntiles = has_b ? 2 : 1;
+      // Descriptors: the high word is a constant, a k-step adds to the low
+      // word (fewer instructions per MMA for the one issuing thread).
+      constexpr uint32_t kHi = smem_desc_sw128_hi(1024);
       auto issue_s = [&](int t, int j) {
-        const uint32_t q_addr = sbase + C::OFF_Q + t * C::NPQ * C::PANEL;
-        const uint32_t k_addr = sbase + C::OFF_K + (j % KS) * C::K_STAGE;
+        const uint32_t qd = smem_desc_sw128_lo(sbase + C::OFF_Q + t * C::NPQ * C::PANEL, 16);
+        const uint32_t kd = smem_desc_sw128_lo(sbase + C::OFF_K + (j % KS) * C::K_STAGE, 16);
 #pragma unroll
         for (int ks = 0; ks < C::S_KSTEPS; ++ks) {
-          const uint32_t off = (ks / C::KSTEPS_PER_PANEL) * C::PANEL + (ks % C::KSTEPS_PER_PANEL) * 32;
-          tc_mma_f16(tmem + C::tm_s(t), smem_desc_sw128(q_addr + off, 16, 1024),
-                     smem_desc_sw128(k_addr + off, 16, 1024), C::IDESC_S, ks > 0 ? 1u : 0u);
+          const uint32_t off =
+              ((ks / C::KSTEPS_PER_PANEL) * C::PANEL + (ks % C::KSTEPS_PER_PANEL) * 32) >> 4;
+          tc_mma_f16(tmem + C::tm_s(t), smem_desc_join(qd + off, kHi), smem_desc_join(kd + off, kHi),
+                     C::IDESC_S, ks > 0 ? 1u : 0u);
         }
         tc_commit(s_full + 8 * t);
       };
       auto issue_pv = [&](int t, int j) {
-        const uint32_t v_addr = sbase + C::OFF_V + (j % VS) * C::V_STAGE;
+        const uint32_t vd = smem_desc_sw128_lo(sbase + C::OFF_V + (j % VS) * C::V_STAGE, C::PANEL);
 #pragma unroll
         for (int ks = 0; ks < C::PV_KSTEPS; ++ks)
           tc_mma_f16_ts(tmem + C::tm_o(t), tmem + C::tm_s(t) + ks * 8,
-                        smem_desc_sw128(v_addr + ks * C::UMMA_K * 128, C::PANEL, 1024), C::IDESC_PV,
+                        smem_desc_join(vd + ((ks * C::UMMA_K * 128) >> 4), kHi), C::IDESC_PV,
                         (j > 0 || ks > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(q_full, 0, p.err, abort_flag) && mbar_wait(k_full, 0, p.err, abort_flag);

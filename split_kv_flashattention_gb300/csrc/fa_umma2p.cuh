@@ -384,23 +384,26 @@ __global__ void __launch_bounds__(384, 1)
         // to the low word.  This single thread issues every MMA of the CTA
         // while sharing its scheduler with two softmax warps, so its
         // instruction count per MMA shows in the tensor pipe's idle time.
+        constexpr uint32_t kHiKmaj = smem_desc_sw128_hi(1024);  // Q, K: K-major
+        constexpr uint32_t kHiV = smem_desc_sw128_hi(1024);     // V: MN-major
         auto issue_s = [&](int t, int kst) {
-          const uint64_t qd = smem_desc_sw128(sbase + C::OFF_Q + t * C::NPQ * C::PANEL, 16, 1024);
-          const uint64_t kd = smem_desc_sw128(sbase + C::OFF_K + kst * C::K_STAGE, 16, 1024);
+          const uint32_t qd = smem_desc_sw128_lo(sbase + C::OFF_Q + t * C::NPQ * C::PANEL, 16);
+          const uint32_t kd = smem_desc_sw128_lo(sbase + C::OFF_K + kst * C::K_STAGE, 16);
 #pragma unroll
           for (int ks = 0; ks < C::S_KSTEPS; ++ks) {
             const uint32_t off =
                 ((ks / C::KSTEPS_PER_PANEL) * C::PANEL + (ks % C::KSTEPS_PER_PANEL) * 32) >> 4;
-            tc_mma_f16(tmem + C::tm_s(t), qd + off, kd + off, C::IDESC_S, ks > 0 ? 1u : 0u);
+            tc_mma_f16(tmem + C::tm_s(t), smem_desc_join(qd + off, kHiKmaj),
+                       smem_desc_join(kd + off, kHiKmaj), C::IDESC_S, ks > 0 ? 1u : 0u);
           }
           tc_commit(s_full + 8 * t);
         };
         auto issue_pv = [&](int t, int vst, bool first) {
-          const uint64_t vd = smem_desc_sw128(sbase + C::OFF_V + vst * C::V_STAGE, C::PANEL, 1024);
+          const uint32_t vd = smem_desc_sw128_lo(sbase + C::OFF_V + vst * C::V_STAGE, C::PANEL);
 #pragma unroll
           for (int ks = 0; ks < C::PV_KSTEPS; ++ks)
             tc_mma_f16_ts(tmem + C::tm_o(t), tmem + C::tm_s(t) + ks * 8,
-                          vd + ((ks * C::UMMA_K * 128) >> 4), C::IDESC_PV,
+                          smem_desc_join(vd + ((ks * C::UMMA_K * 128) >> 4), kHiV), C::IDESC_PV,
                           (!first || ks > 0) ? 1u : 0u);
         };
         // Running counts: Q tiles and K/V blocks consumed, ring entries read;

@@ -555,11 +555,11 @@ def test_running_max_jumps_between_blocks(kernel, growth, causal):
 
 
 # ----------------------------------------- persistent two-tile kernel (AUTO)
-# One split, 16-bit, d <= 128, more than 128 rows per KV head, no mask: AUTO
-# runs the persistent form, which walks a per-CTA tile list (masked cases run
-# the non-persistent kernel and are covered here as well).  Its arithmetic is the
-# two-tile kernel's, so besides the oracle check its output must equal that
-# kernel's bit for bit.
+# One split, 16-bit, d <= 128, more than 128 rows per KV head, with or without
+# a mask: AUTO runs the persistent form, which walks a per-CTA tile list (one
+# instantiation for calls with a causal or window mask, one without).  Its
+# arithmetic is the two-tile kernel's, so besides the oracle check its output
+# must equal that kernel's bit for bit.
 #
 # Rows that see only one or two keys make O a mix of very few V rows with
 # weights rounded to bf16 for the PV MMA; with O rounded to bf16 too, the
@@ -644,19 +644,28 @@ def test_persistent_prefill_out_not_32_byte_aligned(causal):
     assert np.array_equal(out, out2, equal_nan=True) and np.array_equal(lse, lse2, equal_nan=True)
 
 
-def test_persistent_prefill_running_max_jumps():
+@pytest.mark.parametrize("growth", ["moderate", "extreme"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_persistent_prefill_running_max_jumps(growth, causal):
+    """Both instantiations of the persistent kernel.  Its softmax first
+    takes a block's exponentials against the running max and falls back to a
+    pass with the block max when a row sum exceeds 2^8; scaled key blocks
+    make that fallback run, with sums that overflow to inf in the extreme
+    case."""
     lens = [700, 300, 520]
     inp = _quarter_v(make_inputs(lens, lens, 2, 2, 128, 128, "bf16", seed=44))
+    factors = [1.0, 1.0, 8.0, 8.0, 40.0, 1.0] if growth == "moderate" else [1.0, 200.0, 1.0, 1.0, 1.0, 1.0]
     k = inp.k.float()
     cu = inp.cu_seqlens_k.tolist()
     for b in range(len(lens)):
-        for blk, f in enumerate([1.0, 1.0, 8.0, 8.0, 40.0, 1.0]):
+        for blk, f in enumerate(factors):
             r0, r1 = cu[b] + 128 * blk, min(cu[b + 1], cu[b] + 128 * blk + 128)
             if r0 < r1:
                 k[r0:r1] *= f
     inp.k = k.to(inp.k.dtype)
-    out, lse = run_gpu(inp, causal=True, num_splits=1)
-    o_ref, l_ref = reference(inp, 0.0, True)
+    out, lse = run_gpu(inp, causal=causal, num_splits=1)
+    assert fa.fa_debug_last_kernel() == fa.FA_KID_UMMA2_PERSISTENT
+    o_ref, l_ref = reference(inp, 0.0, causal)
     assert_close(inp, out, lse, o_ref, l_ref)
 
 

@@ -282,20 +282,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// The same descriptor in two words.  For fixed offsets only the low word
-// (start address and leading byte offset) depends on the address, so an
-// issue loop keeps the high word in one register and steps the low word:
-// desc(saddr + off) = desc(saddr) + off / 16 while saddr + off < 256 KB.
-__host__ __device__ constexpr uint32_t smem_desc_sw128_hi(uint32_t sbo) {
-  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
-}
-__device__ __forceinline__ uint32_t smem_desc_sw128_lo(uint32_t saddr, uint32_t lbo) {
-  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
-}
-__device__ __forceinline__ uint64_t smem_desc_join(uint32_t lo, uint32_t hi) {
-  return ((uint64_t)hi << 32) | lo;
-}
-
 // Instruction descriptor of tcgen05.mma kind::f16 / kind::f8f6f4 with an
 // fp32 accumulator: a/b format codes (f16: 0 = fp16, 1 = bf16; f8f6f4:
 // 0 = e4m3) in bits 7-9 / 10-12, operand majors (0 = K-major, 1 = MN-major)

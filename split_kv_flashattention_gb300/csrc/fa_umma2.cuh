@@ -32,6 +32,21 @@
 
 namespace fa {
 
+// The shared-memory descriptor of fa_ptx.cuh (smem_desc_sw128) in two words.  For fixed offsets only the low word
+// (start address and leading byte offset) depends on the address, so an
+// issue loop keeps the high word in one register and steps the low word:
+// desc(saddr + off) = desc(saddr) + off / 16 while saddr + off < 256 KB.
+__host__ __device__ constexpr uint32_t smem_desc_sw128_hi(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint32_t smem_desc_sw128_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ uint64_t smem_desc_join(uint32_t lo, uint32_t hi) {
+  return ((uint64_t)hi << 32) | lo;
+}
+
+
 // Whether the two softmax warpgroups strictly alternate (measured slower on
 // GB300 than letting both run: each tile's softmax then has only one warp
 // per SM sub-partition to hide latency with).

@@ -7,11 +7,20 @@ flash-attention PR "[Cute,Fwd,Sm100] Support q_stage=1 for inference",
 "Benchmarks").  One step = one pass of the whole path: the split partial
 kernel plus the combine kernel.  The metric is HBM throughput in TB/s with
 the bytes counted as that page counts them (K + V + Q + O at the storage
-width), divided by the device time of a step.
+width), divided by the device time of a step.  The K timed steps are one
+CUDA graph of K library calls, replayed once.
+
+The default line also carries flat fields for every configuration of the
+metric (cfg1_* tiny decode, cfg2_* the long-decode split sweep 1..128 and
+auto, cfg3_* batched GQA decode, cfg4_* the FP8 cached prefix at 16384 and
+11008 keys, cfg5_* varlen prefill in bf16/fp16, H_kv 16/4, no mask/causal),
+each the median of 7 rounds of 100 CUDA-graph replays of one call (the
+timing of aiter PR "[FlyDSL] Enable FP8 FMHA split-K for short cached-prefix
+queries"), with a roofline fraction against the measured peaks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload long_decode|gqa_decode|fp8_prefix|fp8_prefix_11k]
-                  [--num-splits S] [--kernel auto|simt|umma]
+                  [--workload NAME] [--num-splits S] [--kernel auto|simt|umma|umma2]
+                  [--no-configs] [--no-cpu-baseline]
 
 With N > 1 (torchrun) every rank runs its own replica of the workload
 (independent problems: weak scaling, no collective on the data path) and
@@ -108,48 +117,158 @@ def measured_tensor_peak():
         return 1900.0, 1700.0, "fallback"
 
 
-def prefill_secondary(fa, dev, steps, warmup):
-    """Varlen prefill TFLOPS (the metric's second part) for no-mask and causal."""
-    res = {}
-    peak, _, src = measured_tensor_peak()
-    for name in ("prefill", "prefill_causal"):
-        spec = WORKLOADS[name]
-        inp = workload(spec["name"], device=str(dev), **spec["kw"])
-        causal = spec["causal"]
-        out = torch.empty((inp.q.shape[0], inp.h_q, inp.d_v), dtype=inp.q.dtype, device=dev)
-        lse = torch.empty((inp.h_q, inp.q.shape[0]), dtype=torch.float32, device=dev)
-        cq, ck = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev)
-        stream = torch.cuda.current_stream(dev)
-        ws_bytes = fa.fa_fwd_splitkv_workspace_size(inp.batch, inp.max_seqlen_q, inp.h_q, inp.h_kv,
-                                                   inp.d_v, 0)
-        ws = torch.empty(max(ws_bytes, 16) // 4, dtype=torch.float32, device=dev) if ws_bytes else None
+# ----------------------------------------------------------------------------
+# Graph-replay timing of the five configurations (flat fields of the line)
 
-        def step():
-            fa.fa_fwd_splitkv_ex(inp.q, inp.k, inp.v, cq, ck, inp.max_seqlen_q, out, lse, ws,
-                                 0.0, causal, -1, 0, None, None, None, 0, stream)
-        for _ in range(warmup):
-            step()
-        torch.cuda.synchronize(dev)
-        # inputs (201 MB) are less than twice the L2: overwrite it between
-        # steps, outside the timed spans
-        flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(steps)]
-        for a, b in evs:
-            flush_buf.zero_()
-            a.record(stream)
-            step()
-            b.record(stream)
-        torch.cuda.synchronize(dev)
-        ms = sum(a.elapsed_time(b) for a, b in evs) / steps
-        del flush_buf
-        tf = flops(inp, causal) / (ms * 1e-3) / 1e12
-        res[name] = {"ms": ms, "tflops": tf, "frac": tf / peak, "flops": flops(inp, causal)}
-    res["peak_tflops"] = peak
-    res["peak_source"] = src + " bf16 dense (burst)"
-    res["workload"] = WORKLOADS["prefill"]["desc"].replace(", no mask", "")
-    res["l2"] = "L2 overwritten between steps (256 MB write, untimed)"
-    return res
+ROUNDS, REPS = 7, 100
+SWEEP_SPLITS = (1, 2, 4, 8, 16, 32, 64, 128)
+
+
+class Case:
+    """One workload set up for timing: `copies` copies of its inputs (same
+    values, distinct memory) so that consecutive calls of a replayed graph
+    read inputs that are not in L2; shared outputs and workspace."""
+
+    def __init__(self, fa, dev, spec, num_splits=0, flags=0, rotate=True, kw_extra=None):
+        kw = dict(spec["kw"])
+        kw.update(kw_extra or {})
+        self.spec = spec
+        self.fa = fa
+        self.inp = inp = workload(spec["name"], device=str(dev), **kw)
+        self.causal = spec.get("causal", False)
+        self.num_splits = num_splits
+        self.flags = flags
+        self.copies = [(inp.q, inp.k, inp.v)]
+        self.in_bytes = sum(x.numel() * x.element_size() for x in self.copies[0])
+        for _ in range(copies_for(self.in_bytes) - 1 if rotate else 0):
+            self.copies.append((inp.q.clone(), inp.k.clone(), inp.v.clone()))
+        self.cq, self.ck = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev)
+        out_dtype = torch.bfloat16 if inp.dtype == "e4m3" else inp.q.dtype
+        self.out = torch.empty((inp.q.shape[0], inp.h_q, inp.d_v), dtype=out_dtype, device=dev)
+        self.lse = torch.empty((inp.h_q, inp.q.shape[0]), dtype=torch.float32, device=dev)
+        self.ns, _ = fa.fa_plan(inp.batch, inp.max_seqlen_q, inp.h_q, inp.h_kv, num_splits)
+        nbytes = fa.fa_fwd_splitkv_workspace_size(inp.batch, inp.max_seqlen_q, inp.h_q, inp.h_kv,
+                                                  inp.d_v, num_splits)
+        self.ws = (torch.empty(max(nbytes, 16) // 4, dtype=torch.float32, device=dev)
+                   if nbytes else None)
+        self.dq = self.dk = self.dv = None
+        if inp.dtype == "e4m3":
+            self.dq = torch.tensor([inp.descale_q], dtype=torch.float32, device=dev)
+            self.dk = torch.tensor([inp.descale_k], dtype=torch.float32, device=dev)
+            self.dv = torch.tensor([inp.descale_v], dtype=torch.float32, device=dev)
+
+    def call(self, i, stream, extra_flags=0):
+        q, k, v = self.copies[i % len(self.copies)]
+        self.fa.fa_fwd_splitkv_ex(q, k, v, self.cq, self.ck, self.inp.max_seqlen_q, self.out,
+                                  self.lse, self.ws, 0.0, self.causal, -1, self.num_splits,
+                                  self.dq, self.dk, self.dv, self.flags | extra_flags, stream)
+
+
+def copies_for(in_bytes):
+    """Input copies a replayed graph cycles through: inputs of 256 MB (twice
+    the L2) or more need none; smaller ones get enough copies that the calls
+    between two uses of one copy read at least 256 MB."""
+    if in_bytes >= L2_FLUSH_BYTES:
+        return 1
+    return min(512, -(-L2_FLUSH_BYTES // max(1, in_bytes)) + 1)
+
+
+def graph_times(case, dev, rounds=ROUNDS, reps=REPS, extra_flags=0):
+    """Per-call milliseconds of `rounds` replays of one CUDA graph holding
+    `reps` calls (cycling through the case's input copies), after two warm
+    replays; CUDA events on the replay stream."""
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        for i in range(3):
+            case.call(i, s, extra_flags)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(reps):
+            case.call(i, s, extra_flags)
+    times = []
+    with torch.cuda.stream(s):
+        for r in range(rounds + 2):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+            s.synchronize()
+            if r >= 2:
+                times.append(e0.elapsed_time(e1) / reps)
+    del g
+    return times
+
+
+def metric_bytes(inp):
+    """K + V + Q + O at storage width (the flash-attention PR's `bw`)."""
+    es = 1 if inp.dtype == "e4m3" else 2
+    return (inp.k.shape[0] * inp.h_kv * (inp.d_qk + inp.d_v) * es
+            + inp.q.shape[0] * inp.h_q * inp.d_qk * es + inp.q.shape[0] * inp.h_q * inp.d_v * 2)
+
+
+CONFIG_FIELDS = [
+    # (field prefix, workload spec, num_splits, kind)
+    ("cfg1_tiny_decode", dict(name="tiny_decode", kw={}), 4, "latency"),
+    ("cfg3_gqa_decode", dict(name="gqa_decode", kw={}), 0, "hbm"),
+    ("cfg4_fp8_prefix_16384", dict(name="fp8_prefix", kw={"kv": 16384}), 0, "hbm"),
+    ("cfg4_fp8_prefix_11008", dict(name="fp8_prefix", kw={"kv": 11008}), 0, "hbm"),
+] + [
+    (f"cfg5_prefill_{dt}_hkv{hkv}_{'causal' if c else 'nomask'}",
+     dict(name="prefill", kw={"h_kv": hkv, "dtype": dt}, causal=c), 0, "tensor")
+    for dt in ("bf16", "fp16") for hkv in (16, 4) for c in (False, True)
+]
+
+
+def config_fields(fa, dev, hbm_peak, tensor_peak):
+    """Flat fields for the five configurations: the long-decode split sweep,
+    tiny decode, GQA decode, the FP8 cached prefix at both key lengths and the
+    varlen prefill variants; each the median of ROUNDS rounds of REPS
+    CUDA-graph replays of one library call (partial + combine)."""
+    out = {}
+
+    def med(ts):
+        return statistics.median(ts)
+
+    sweep = [("cfg2_long_decode_auto", 0)] + [(f"cfg2_long_decode_ns{n}", n) for n in SWEEP_SPLITS]
+    case = Case(fa, dev, dict(name="long_decode", kw={}))
+    mb = metric_bytes(case.inp)
+    for name, ns in sweep:
+        case.num_splits = ns
+        nbytes = fa.fa_fwd_splitkv_workspace_size(case.inp.batch, 1, case.inp.h_q, case.inp.h_kv,
+                                                  case.inp.d_v, ns)
+        if case.ws is None or case.ws.numel() * 4 < nbytes:
+            case.ws = torch.empty(max(nbytes, 16) // 4, dtype=torch.float32, device=dev)
+        ms = med(graph_times(case, dev))
+        out[name + "_us"] = ms * 1e3
+        out[name + "_tbs"] = mb / (ms * 1e-3) / 1e12
+        out[name + "_frac"] = mb / (ms * 1e-3) / 1e9 / hbm_peak
+        if ns == 0:
+            out[name + "_ns"] = fa.fa_plan(1, 1, 32, 32, 0)[0]
+    del case
+    torch.cuda.empty_cache()
+
+    for prefix, spec, ns, kind in CONFIG_FIELDS:
+        case = Case(fa, dev, spec, num_splits=ns)
+        ms = med(graph_times(case, dev))
+        out[prefix + "_us"] = ms * 1e3
+        if kind == "hbm":
+            mb = metric_bytes(case.inp)
+            out[prefix + "_tbs"] = mb / (ms * 1e-3) / 1e12
+            out[prefix + "_frac"] = mb / (ms * 1e-3) / 1e9 / hbm_peak
+            out[prefix + "_ns"] = case.ns
+        elif kind == "tensor":
+            tf = flops(case.inp, case.causal) / (ms * 1e-3) / 1e12
+            out[prefix + "_tflops"] = tf
+            out[prefix + "_frac"] = tf / tensor_peak
+        del case
+        torch.cuda.empty_cache()
+    out["cfg_timing"] = (f"median of {ROUNDS} rounds x {REPS} CUDA-graph replays of one library call "
+                         "(partial + combine), CUDA events; inputs under 256 MB rotated over copies so "
+                         "that 256 MB (twice the L2) is read between two uses of one copy")
+    out["cfg_frac_peaks"] = {"hbm_gbs": hbm_peak, "bf16_tflops": tensor_peak}
+    return out
 
 
 def max_over_ranks(x: float, world: int, device=None) -> float:
@@ -203,8 +322,8 @@ def parse():
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "umma", "umma2"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-prefill", action="store_true",
-                    help="skip the varlen prefill TFLOPS measurement of the default line")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration fields of the default line")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--kv", type=int, default=0, help="override the key length (long_decode)")
     return ap.parse_args()
@@ -275,7 +394,7 @@ def profiled_traffic(kernel_tag, workload_name):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
@@ -290,7 +409,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception as e:  # pragma: no cover
             self.error = str(e)
@@ -316,7 +435,13 @@ class ClockSampler:
         if self.error or not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
                     "note": self.error or "no nvidia-smi samples"}
-        inside = [p for t, p in self.samples if t0 <= t <= t1] or [p for _, p in self.samples]
+        # a window shorter than the sampling interval is widened to the
+        # samples around it, and the line says so
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        widened = 0.0
+        while not inside and widened < 2.0:
+            widened += 0.1
+            inside = [p for t, p in self.samples if t0 - widened <= t <= t1 + widened]
 
         def num(x):
             try:
@@ -327,9 +452,12 @@ class ClockSampler:
         mx = [num(p[1]) for p in inside if num(p[1]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for p in inside for i in range(4) if p[3 + i] == "Active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(inside)}
+        res = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+               "samples": len(inside), "window_s": round(t1 - t0, 4)}
+        if widened:
+            res["widened_s"] = round(widened, 1)
+        return res
 
 
 def cpu_baseline(inp_cpu, budget_s=12.0, heads=2, causal=False, kind="hbm"):
@@ -428,136 +556,111 @@ def main():
 
     kernel_flag = {"auto": fa.FA_KERNEL_AUTO, "simt": fa.FA_KERNEL_SIMT,
                    "umma": fa.FA_KERNEL_UMMA, "umma2": fa.FA_KERNEL_UMMA2}[args.kernel]
-    kw = dict(spec["kw"])
-    if args.kv:
-        kw["kv"] = args.kv
-    inp = workload(spec["name"], device=str(dev), **kw)
-    q, k, v = inp.q, inp.k, inp.v
-    cq, ck = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev)
+    kw = {"kv": args.kv} if args.kv else {}
     paged = spec.get("paged", 0)
+    case = Case(fa, dev, spec, num_splits=args.num_splits, flags=kernel_flag, rotate=not paged,
+                kw_extra=kw)
+    inp = case.inp
+    ns = case.ns
+    stream = torch.cuda.current_stream(dev)
     if paged:
         # the same keys, scattered into a shuffled page pool
         kc, vc, bt, sk = to_paged(inp, paged, dev)
-    out_dtype = torch.bfloat16 if inp.dtype == "e4m3" else q.dtype
-    out = torch.empty((q.shape[0], inp.h_q, inp.d_v), dtype=out_dtype, device=dev)
-    lse = torch.empty((inp.h_q, q.shape[0]), dtype=torch.float32, device=dev)
-    ns, _ = fa.fa_plan(inp.batch, inp.max_seqlen_q, inp.h_q, inp.h_kv, args.num_splits)
-    ws_bytes = fa.fa_fwd_splitkv_workspace_size(inp.batch, inp.max_seqlen_q, inp.h_q, inp.h_kv,
-                                               inp.d_v, args.num_splits)
-    ws = torch.empty(max(ws_bytes, 16) // 4, dtype=torch.float32, device=dev) if ws_bytes else None
-    dq = dk = dv = None
-    if inp.dtype == "e4m3":
-        dq = torch.tensor([inp.descale_q], dtype=torch.float32, device=dev)
-        dk = torch.tensor([inp.descale_k], dtype=torch.float32, device=dev)
-        dv = torch.tensor([inp.descale_v], dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    def call(flags):
-        if paged:
-            fa.fa_fwd_splitkv_paged(q, kc, vc, cq, sk, bt, inp.max_seqlen_q, out, lse, ws, 0.0,
-                                    causal, -1, args.num_splits, dq, dk, dv, flags, stream)
-            return
-        fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, inp.max_seqlen_q, out, lse, ws, 0.0, causal, -1,
-                             args.num_splits, dq, dk, dv, flags, stream)
 
-    def partial():
-        call(kernel_flag | fa.FA_RUN_PARTIAL_ONLY)
+        def call(i, s, extra=0):
+            fa.fa_fwd_splitkv_paged(inp.q, kc, vc, case.cq, sk, bt, inp.max_seqlen_q, case.out,
+                                    case.lse, case.ws, 0.0, causal, -1, args.num_splits, case.dq,
+                                    case.dk, case.dv, kernel_flag | extra, s)
+    else:
+        call = case.call
 
-    def combine():
-        if ns > 1:
-            call(kernel_flag | fa.FA_RUN_COMBINE_ONLY)
+    def graph_of(n, extra):
+        """A CUDA graph of n calls (cycling through the input copies)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for i in range(n):
+                call(i, side, extra)
+        return g
 
     sampler = ClockSampler(local_rank)
     sampler.start()
-    for _ in range(args.warmup):
-        partial()
-        combine()
+    for i in range(args.warmup):
+        call(i, stream)
     torch.cuda.synchronize(dev)
     if fa.fa_get_device_error(clear=True) != 0:
         raise RuntimeError("device error during warm-up")
     # the partial kernel the library chose (the last call above enqueued it)
-    partial()
     kern_tag = KERNEL_TAGS[fa.fa_debug_last_kernel()]
-    torch.cuda.synchronize(dev)
 
-    # Timed region: K whole steps (partial + combine, as one call makes them,
-    # so the combine's programmatic launch overlaps the partial's tail).
-    def timed(fn, n):
+    # Timed region: exactly K steps (one library call each: partial kernel,
+    # then the combine as its programmatic dependent when ns > 1), captured
+    # in one CUDA graph so that no host work sits between them, replayed
+    # once between a barrier and a synchronize.  Inputs under 256 MB rotate
+    # over copies, so every step reads inputs that are not in L2.
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    graphs = {"step": graph_of(args.steps, 0),
+              "partial": graph_of(args.steps, fa.FA_RUN_PARTIAL_ONLY)}
+    if ns > 1:
+        graphs["combine"] = graph_of(args.steps, fa.FA_RUN_COMBINE_ONLY)
+
+    def replay(g):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
-        e0.record(stream)
-        for _ in range(n):
-            fn()
-        e1.record(stream)
+        with torch.cuda.stream(side):
+            e0.record(side)
+            g.replay()
+            e1.record(side)
         torch.cuda.synchronize(dev)
         if world > 1:
             torch.distributed.barrier()
         return e0.elapsed_time(e1)
 
-    # Workloads that fit in L2 are timed step by step with L2 overwritten in
-    # between (outside the timed spans); larger ones run back to back.
-    in_bytes = sum(x.numel() * x.element_size() for x in (q, k, v))
-    flush_l2 = in_bytes < L2_FLUSH_BYTES
-    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if flush_l2 else None
-
-    def timed_flushed(fn, n):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(n)]
-        if world > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize(dev)
-        for a, b in evs:
-            flush_buf.zero_()
-            a.record(stream)
-            fn()
-            b.record(stream)
-        torch.cuda.synchronize(dev)
-        if world > 1:
-            torch.distributed.barrier()
-        return sum(a.elapsed_time(b) for a, b in evs)
-
-    run = timed_flushed if flush_l2 else timed
+    # the partial graph replays once untimed first: its first replay pays
+    # the graph upload
+    replay(graphs["partial"])
     t_wall0 = time.time()
-    total_ms = run(lambda: call(kernel_flag), args.steps)
+    total_ms = replay(graphs["step"])
     t_wall1 = time.time()
     # The dominant (partial) kernel alone, K launches, for its roofline; then
     # the combine alone over the same workspace.
-    partial_ms = run(partial, args.steps) / args.steps
-    combine_ms = run(combine, args.steps) / args.steps if ns > 1 else 0.0
-    sampler.stop()
-    clocks = sampler.summary(t_wall0, t_wall1)
+    partial_ms = replay(graphs["partial"]) / args.steps
+    combine_ms = replay(graphs["combine"]) / args.steps if ns > 1 else 0.0
     err = fa.fa_get_device_error(clear=True)
     if err != 0:
         raise RuntimeError(f"device error {fa.fa_status_string(err)}")
+    del graphs
 
     total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
-    metric_bytes, partial_bytes = byte_counts(inp, ns)
+    metric_b, partial_bytes = byte_counts(inp, ns)
     work_flops = flops(inp, causal)
     if kind == "tensor":
         unit = "TFLOPS"
         value = job_throughput(work_flops, world, ms_per_step)
     else:
         unit = "TB/s"
-        value = job_throughput(metric_bytes, world, ms_per_step)
+        value = job_throughput(metric_b, world, ms_per_step)
 
     # ---- end to end through the public call with host buffers
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    q, k, v = case.copies[0]
     # the step's inputs: Q and cu_seqlens_q, and K/V with their index arrays
-    dev_in = [q, cq] + ([kc, vc, bt, sk] if paged else [k, v, ck])
+    dev_in = [q, case.cq] + ([kc, vc, bt, sk] if paged else [k, v, case.ck])
     host_in = [x.cpu().pin_memory() for x in dev_in]
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h_out = torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory()
+    h_lse = torch.empty(case.lse.shape, dtype=case.lse.dtype).pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in host_in)
     d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
 
     def e2e_step():
         for d_t, h_t in zip(dev_in, host_in):
             d_t.copy_(h_t, non_blocking=True)
-        call(kernel_flag)
-        h_out.copy_(out, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        call(0, stream)
+        h_out.copy_(case.out, non_blocking=True)
+        h_lse.copy_(case.lse, non_blocking=True)
 
     e2e_step()
     torch.cuda.synchronize(dev)
@@ -570,34 +673,46 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
-    e2e_value = job_throughput(work_flops if kind == "tensor" else metric_bytes, world, e2e_ms)
+    e2e_value = job_throughput(work_flops if kind == "tensor" else metric_b, world, e2e_ms)
+    del case, host_in
+    torch.cuda.empty_cache()
 
-    secondary = None
-    if kind == "hbm" and world == 1 and not args.no_prefill:
-        secondary = prefill_secondary(fa, dev, steps=max(3, min(args.steps, 30)),
-                                      warmup=max(3, min(args.warmup, 5)))
+    peak_gbs, peak_src = measured_peaks()
+    tpeak, _, tpeak_src = measured_tensor_peak()
+    cfg = None
+    t_cfg0 = t_cfg1 = None
+    if world == 1 and not args.no_configs and args.workload == "long_decode" and not args.kv:
+        t_cfg0 = time.time()
+        cfg = config_fields(fa, dev, peak_gbs, tpeak)
+        t_cfg1 = time.time()
+        if fa.fa_get_device_error(clear=True) != 0:
+            raise RuntimeError("device error during the configuration sweep")
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    if t_cfg0 is not None:
+        clocks["all_timed_regions"] = sampler.summary(t_wall0, t_cfg1)
 
     if rank == 0:
         if kind == "tensor":
-            peak, peak_sus, src = measured_tensor_peak()
             achieved = work_flops / (partial_ms * 1e-3) / 1e12
             same_rate = "" if inp.dtype == "bf16" else f"; {inp.dtype} dense at the bf16 nominal rate (1:1)"
-            roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "peak_source": src + " bf16 dense (burst)" + same_rate,
+            roof = {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
+                    "frac": achieved / tpeak,
+                    "peak_source": tpeak_src + " bf16 dense (burst)" + same_rate,
                     "traffic": profiled_traffic(kern_tag, args.workload),
                     "kernel": f"{kern_tag} partial kernel", "partial_ms": partial_ms,
-                    "timing": "K partial-only launches, CUDA events",
+                    "timing": "K partial-only launches in one CUDA graph, CUDA events",
                     "algorithmic_flops_per_launch": work_flops}
         else:
-            peak_gbs, peak_src = measured_peaks()
             achieved_gbs = partial_bytes / (partial_ms * 1e-3) / 1e9
             roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": peak_gbs, "unit": "GB/s",
                     "frac": achieved_gbs / peak_gbs, "peak_source": peak_src,
                     "traffic": profiled_traffic(kern_tag, args.workload),
                     "kernel": f"{kern_tag} partial kernel", "partial_ms": partial_ms,
                     "combine_ms": combine_ms,
-                    "timing": "K partial-only launches, CUDA events",
+                    "timing": "K partial-only launches in one CUDA graph, CUDA events",
                     "algorithmic_bytes_per_launch": partial_bytes}
+        in_bytes = sum(x.numel() * x.element_size() for x in (inp.q, inp.k, inp.v))
         line = {
             "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -605,8 +720,11 @@ def main():
             "dtype": "bf16" if inp.dtype == "bf16" else inp.dtype, "data": "synthetic",
             "config": {"workload": spec["desc"], "num_splits": ns,
                        "num_splits_requested": args.num_splits, "kernel": kern_tag,
-                       "l2": ("L2 overwritten between steps (256 MB write, untimed); Q+K+V %.3f GB"
-                              if flush_l2 else "inputs larger than L2 (Q+K+V %.2f GB)") % (in_bytes / 1e9),
+                       "l2": ("inputs larger than L2 (Q+K+V %.2f GB)" % (in_bytes / 1e9)
+                              if in_bytes >= L2_FLUSH_BYTES else
+                              "Q+K+V %.3f GB rotated over %d copies (256 MB read between two "
+                              "uses of one copy)" % (in_bytes / 1e9, copies_for(in_bytes))),
+                       "timing": "K steps captured in one CUDA graph, replayed once; CUDA events",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roof,
             "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
@@ -614,8 +732,8 @@ def main():
             "gpu_launches": args.steps * (2 if ns > 1 else 1),
             "clocks": clocks,
         }
-        if secondary is not None:
-            line["prefill"] = secondary
+        if cfg is not None:
+            line.update(cfg)
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline(inp_host(inp), causal=causal, kind=kind)
         print(json.dumps(line), flush=True)

@@ -91,7 +91,13 @@ typedef enum {
 #define FA_RUN_COMBINE_ONLY 8
 
 /*
- * fa_fwd_splitkv_ex -- split-KV attention forward (flash-decoding).
+ * fa_fwd_splitkv_ex -- split-KV attention forward (flash-decoding):
+ * flash-attention PR "[Cute,Fwd,Sm100] Support q_stage=1 for inference"
+ * (description: split KV over CTAs of one 128-row query tile), aiter PR
+ * "[FlyDSL] Enable FP8 FMHA split-K for short cached-prefix queries"
+ * (description: automatic and explicit splits, return_lse, FP8) and cutlass
+ * "Adds variable sequence lengths to the Hopper CuTe DSL FMHA example"
+ * ("Interface": cu_seqlens, packed varlen, GQA).
  *
  *  q, k, v        device inputs, layouts above, element type in_dtype.
  *  cu_seqlens_q/k device int32 [batch+1].
@@ -171,8 +177,18 @@ FA_API int fa_fwd_splitkv_paged(const void* q, const void* k_cache, const void* 
                                 int out_dtype, const float* descale_q, const float* descale_k,
                                 const float* descale_v, int flags, void* stream);
 
-/* bf16 in / bf16 out shorthand of fa_fwd_splitkv_ex with automatic kernel
- * selection; the workspace is trusted to be large enough. */
+/*
+ * fa_fwd_splitkv -- bf16 in / bf16 out shorthand of fa_fwd_splitkv_ex with
+ * automatic kernel selection: the split-KV forward of flash-attention PR
+ * "[Cute,Fwd,Sm100] Support q_stage=1 for inference" (description: one
+ * 128-row query tile per CTA, split KV on by default) with the automatic or
+ * explicit split count of aiter PR "[FlyDSL] Enable FP8 FMHA split-K for
+ * short cached-prefix queries" (description).  Arguments as in
+ * fa_fwd_splitkv_ex; batch, total_q and total_k are needed because the host
+ * cannot read cu_seqlens without synchronising and the tensor maps must know
+ * where the buffers end.  The workspace is trusted to hold
+ * fa_fwd_splitkv_workspace_size(...) bytes.
+ */
 FA_API int fa_fwd_splitkv(const void* q, const void* k, const void* v, const int* cu_seqlens_q,
                    const int* cu_seqlens_k, int batch, int total_q, int total_k,
                    int max_seqlen_q, int h_q, int h_kv, int d_qk, int d_v, float scale,
@@ -213,28 +229,46 @@ FA_API int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v,
                                   int out_dtype, const float* descale_q, const float* descale_k,
                                   const float* descale_v, int flags, void* stream);
 
-/* Bytes of workspace fa_fwd_splitkv_ex needs for these sizes: the fp32
- * partial outputs [ns, batch*max_seqlen_q, h_q, d_v] followed by the partial
- * LSEs [ns, batch*max_seqlen_q, h_q]; 16 (the persistent kernel's tile
- * counter) when the resolved split count is 1.  num_splits = 0 resolves the
- * automatic count on the current device.  Returns 0 for invalid sizes. */
+/*
+ * fa_fwd_splitkv_workspace_size -- bytes of workspace fa_fwd_splitkv_ex needs
+ * for these sizes.  aiter PR "[FlyDSL] Enable FP8 FMHA split-K for short
+ * cached-prefix queries" (review: automatic split-K "plus a per-call fp32
+ * workspace"; timing note: attention and split combine): the fp32 partial
+ * outputs [ns, batch*max_seqlen_q, h_q, d_v] followed by the partial LSEs
+ * [ns, batch*max_seqlen_q, h_q], indexed by (sequence, query) so that the
+ * host can size them without reading cu_seqlens; 16 bytes (the persistent
+ * kernel's tile counter) when the resolved split count is 1.  num_splits = 0
+ * resolves the automatic count on the current device.  Returns 0 for
+ * invalid sizes.
+ */
 FA_API size_t fa_fwd_splitkv_workspace_size(int batch, int max_seqlen_q, int h_q, int h_kv, int d_v,
                                      int num_splits);
 
 /*
- * fa_plan -- the split planner (host only; no device work).
+ * fa_plan -- the split planner (host only; no device work).  The pages give
+ * its inputs, not its rule: aiter PR "[FlyDSL] Enable FP8 FMHA split-K for
+ * short cached-prefix queries" (description: automatic and explicit split
+ * selection; review: up to 16 splits) and flash-attention PR "[Cute,Fwd,
+ * Sm100] Support q_stage=1 for inference" ("Benchmarks": the num_splits
+ * sweep 1..128 at B=1, Q=1, K=131072, H=32, where too few splits leave SMs
+ * idle).  The rule below is this library's reading.
  * units = batch * h_kv * ceil(max_seqlen_q * (h_q/h_kv) / 128) work units;
  * explicit num_splits > 0 is clipped to 128; with no work or with
  * units >= 2*num_sms the count is 1; otherwise it is the smallest ns in
  * 1..128 whose wave efficiency units*ns / (ceil(units*ns/num_sms)*num_sms)
  * reaches 0.9, else the first most efficient one.  num_sms <= 0 queries the
- * current device.  Writes the split count and the unit count.
+ * current device.  Writes the split count and the unit count (the kernels
+ * decode a linear CTA index, so the launch shape is the unit count times the
+ * split count, or one CTA per SM for the persistent kernel, not a 3-D grid).
  */
 FA_API int fa_plan(int batch, int max_seqlen_q, int h_q, int h_kv, int num_splits, int num_sms,
             int* num_splits_out, int* units_out);
 
 /*
- * fa_debug_split_ranges -- test hook: runs the device-side tile decode for a
+ * fa_debug_split_ranges -- test hook (no counterpart on the pages; it exposes
+ * the key split of flash-attention PR "[Cute,Fwd,Sm100] Support q_stage=1
+ * for inference", description, as the kernels compute it on the device so
+ * that it can be checked bit for bit): runs the device-side tile decode for a
  * tile of `tile_queries` queries and writes, for every (m_block, b, split),
  * the sequence-local key range [k0, k1) the kernels process (k1 <= k0 for an
  * empty split) to ranges_out: device int32 [ceil(max_seqlen_q/tile_queries),
@@ -269,14 +303,17 @@ typedef enum {
  * error, FA_RUN_COMBINE_ONLY, or no sequence). */
 FA_API int fa_debug_last_kernel(void);
 
-/* Sticky device error word of the current device (FA_OK if none).  Waits
- * for the device to finish its work.  clear != 0 resets the word. */
+/* Sticky device error word of the current device (FA_OK if none); no
+ * counterpart on the pages.  Waits for the device to finish its work.
+ * clear != 0 resets the word. */
 FA_API int fa_get_device_error(int clear);
 
-/* Human-readable name of an fa_status value (static string). */
+/* Human-readable name of an fa_status value (static string); no counterpart
+ * on the pages. */
 FA_API const char* fa_status_string(int status);
 
-/* Library version: major*10000 + minor*100 + patch. */
+/* Library version: major*10000 + minor*100 + patch; no counterpart on the
+ * pages. */
 FA_API int fa_version(void);
 
 #ifdef __cplusplus

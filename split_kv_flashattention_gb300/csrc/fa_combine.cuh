@@ -7,8 +7,11 @@
 // O rows (one round of loads for up to 16 splits), forms
 //     M = max_s lse_s,  w_s = exp(lse_s - M),  LSE = M + ln(sum_s w_s)
 // and accumulates O = sum_s (w_s / sum w) * O_s with 128-bit loads, lane l
-// owning columns [l*d_v/32, (l+1)*d_v/32).  Rows whose splits are all empty
-// (M = -inf) get O = 0 and LSE = -inf.
+// owning columns [l*d_v/32, (l+1)*d_v/32).  The row is written with 128-bit
+// stores: lanes convert their columns to the output type and the first lane
+// of each group that makes 16 bytes gathers the group's words by shuffles
+// (d_v = 128, 16-bit: 16 lanes store 8 values each).  Rows whose splits are
+// all empty (M = -inf) get O = 0 and LSE = -inf.
 #pragma once
 
 #include <math_constants.h>
@@ -18,6 +21,50 @@
 #include "fa_ptx.cuh"
 
 namespace fa {
+
+// Output row of one warp (lane l holds columns [l*DPL, (l+1)*DPL)) written
+// with 16-byte stores.  W packed 32-bit words per lane; the first lane of
+// every group of 4/W lanes collects the group's 16 bytes.  The row starts
+// on a 16-byte boundary (O is 16-byte aligned, rows are d_v elements).
+template <int W>
+__device__ __forceinline__ void store_row_16B(uint8_t* row, int lane, const uint32_t* w) {
+  constexpr int G = 4 / W;
+  uint32_t v[4];
+#pragma unroll
+  for (int i = 0; i < W; ++i) v[i] = w[i];
+#pragma unroll
+  for (int g = 1; g < G; ++g)
+#pragma unroll
+    for (int i = 0; i < W; ++i) v[g * W + i] = __shfl_down_sync(0xffffffffu, w[i], g);
+  if ((lane & (G - 1)) == 0)
+    *reinterpret_cast<uint4*>(row + lane * W * 4) = make_uint4(v[0], v[1], v[2], v[3]);
+}
+
+template <int DPL>
+__device__ __forceinline__ void store_combined_row(void* out, size_t row_elem, const float* f,
+                                                   int lane, int out_dtype) {
+  if (out_dtype == kE4M3) {
+    if constexpr (DPL % 4 == 0) {
+      uint32_t w[DPL / 4];
+#pragma unroll
+      for (int i = 0; i < DPL / 4; ++i) {
+        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+            make_float2(f[4 * i], f[4 * i + 1]), __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+            make_float2(f[4 * i + 2], f[4 * i + 3]), __NV_SATFINITE, __NV_E4M3);
+        w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+      }
+      store_row_16B<DPL / 4>(static_cast<uint8_t*>(out) + row_elem, lane, w);
+    } else {
+      store_o<DPL>(out, row_elem + lane * DPL, f, 1.f, out_dtype);
+    }
+  } else {
+    uint32_t w[DPL / 2];
+#pragma unroll
+    for (int i = 0; i < DPL / 2; ++i) w[i] = pack2(f[2 * i], f[2 * i + 1], out_dtype);
+    store_row_16B<DPL / 2>(static_cast<uint8_t*>(out) + row_elem * 2, lane, w);
+  }
+}
 
 template <int DV>
 __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ FwdParams p) {
@@ -128,8 +175,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ Fw
     }
   }
 
-  if (timed_out) return;
-  store_o<DPL>(p.out, ((size_t)t * p.h_q + h) * DV + lane * DPL, acc, 1.f, p.out_dtype);
+  if (__any_sync(0xffffffffu, timed_out)) return;
+  store_combined_row<DPL>(p.out, ((size_t)t * p.h_q + h) * DV, acc, lane, p.out_dtype);
   if (p.lse != nullptr && lane == 0) p.lse[(size_t)h * p.total_q + t] = lse_out;
 }
 

@@ -21,8 +21,8 @@
 //   warps 2-5   one thread per query row (TMEM lane): load the S row, apply
 //               the residual / bottom-right causal / window mask, online
 //               softmax in the exp2 domain, rescale the O row in TMEM when
-//               the running max moves, write P (bf16 / fp16 / e4m3, 128B
-//               swizzled K-major) to shared memory, and finally normalise O
+//               the running max moves, write P (bf16 / fp16 / e4m3) into
+//               TMEM over the S columns it came from, and finally normalise O
 //               and store it (or the fp32 split partial) with row-predicated
 //               vector stores (cutlass "Adds variable sequence lengths to the
 //               Hopper CuTe DSL FMHA example", "Implementation": rows past a
@@ -30,7 +30,7 @@
 //
 // Operand layouts (all 128B-swizzled, 1024-byte aligned, 128-byte rows):
 //   Q  [128 rows][d_qk]  K-major A of S      K [128 keys][d_qk]  K-major B of S
-//   P  [128 rows][128 keys] K-major A of PV  V [128 keys][d_v]   MN-major B of PV
+//   P  [128 rows][128 keys] in TMEM, A of PV  V [128 keys][d_v]  MN-major B of PV
 // each split into 128-byte-wide panels of 128 rows (16 KB).
 #pragma once
 
@@ -53,8 +53,6 @@ struct UmmaCfg {
   static constexpr int NPV = (DV * ES + 127) / 128;        // panels of V
   // P stays in TMEM (over the S columns it came from) as the PV MMA's A
   // operand: 16-bit P two per column, e4m3 P four per column.
-  static constexpr bool P_TMEM = true;
-  static constexpr int NPP = 0;                            // smem panels of P
   static constexpr int UMMA_K = 32 / ES;                   // K elements per MMA
   static constexpr int KSTEPS_PER_PANEL = PANEL_ELEMS / UMMA_K;
   static constexpr int S_KSTEPS = (DQK + UMMA_K - 1) / UMMA_K;
@@ -66,8 +64,7 @@ struct UmmaCfg {
   static constexpr int V_STAGE = NPV * PANEL;
   static constexpr int OFF_K = OFF_Q + NPQ * PANEL;
   static constexpr int OFF_V = OFF_K + KS * K_STAGE;
-  static constexpr int OFF_P = OFF_V + VS * V_STAGE;
-  static constexpr int OFF_BAR = OFF_P + NPP * PANEL;
+  static constexpr int OFF_BAR = OFF_V + VS * V_STAGE;
   // barriers: q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2],
   // p_ready, o_ready, drain
   static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 2 + 3;
@@ -93,46 +90,16 @@ __device__ __forceinline__ void mma_issue(uint32_t d, uint64_t a, uint64_t b, ui
     tc_mma_f16(d, a, b, idesc, acc);
 }
 
-// Packs 8 probabilities into 16 bytes of P (16-bit types) or 16 into 16
-// bytes (e4m3).  With the lazy rescale below a probability is at most
-// 2^kLazy[DT]; e4m3 P is scaled by kP8Scale = 2^(8 - 4) so it stays within
-// e4m3's range (448) while small values keep their leading bits.
 // Lazy rescale threshold (log2 units): the running max used for the
 // exponentials is only raised when a row's true max exceeds it by more
-// than this, so O in TMEM is rarely rescaled.
+// than this, so O in TMEM is rarely rescaled.  With it a probability is at
+// most 2^kThreshold; e4m3 P is scaled by kP8Scale = 2^(8 - 4) so that it
+// stays within e4m3's range (448) while small values keep their leading bits.
 template <int DT>
 struct Lazy {
   static constexpr float kThreshold = DT == kE4M3 ? 4.f : 8.f;
 };
 constexpr float kP8Scale = 16.f;
-
-template <int DT>
-__device__ __forceinline__ uint4 pack_p16(const float* p);
-
-template <>
-__device__ __forceinline__ uint4 pack_p16<kBF16>(const float* p) {
-  return make_uint4(pack2(p[0], p[1], kBF16), pack2(p[2], p[3], kBF16), pack2(p[4], p[5], kBF16),
-                    pack2(p[6], p[7], kBF16));
-}
-template <>
-__device__ __forceinline__ uint4 pack_p16<kFP16>(const float* p) {
-  return make_uint4(pack2(p[0], p[1], kFP16), pack2(p[2], p[3], kFP16), pack2(p[4], p[5], kFP16),
-                    pack2(p[6], p[7], kFP16));
-}
-template <>
-__device__ __forceinline__ uint4 pack_p16<kE4M3>(const float* p) {
-  uint32_t w[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __nv_fp8x2_storage_t lo =
-        __nv_cvt_float2_to_fp8x2(make_float2(p[4 * i] * kP8Scale, p[4 * i + 1] * kP8Scale),
-                                 __NV_SATFINITE, __NV_E4M3);
-    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-        make_float2(p[4 * i + 2] * kP8Scale, p[4 * i + 3] * kP8Scale), __NV_SATFINITE, __NV_E4M3);
-    w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
 
 template <int DT, int DQK, int DV, int KS, int VS>
 __global__ void __launch_bounds__(192, 1)
@@ -288,7 +255,6 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0 && nblk > 0) {
       bool ok = mbar_wait(q_full, 0, p.err, abort_flag);
       const uint32_t q_addr = sbase + C::OFF_Q;
-      const uint32_t p_addr = sbase + C::OFF_P;
       auto issue_s = [&](int j) {
         const int st = j % KS;
         const uint32_t k_addr = sbase + C::OFF_K + st * C::K_STAGE;
@@ -326,18 +292,11 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t b_off = ks * C::UMMA_K * 128;
           const uint64_t v_desc = smem_desc_sw128(v_addr + b_off, C::PANEL, 1024);
           const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
-          if constexpr (C::P_TMEM) {
-            const uint32_t a_t = tmem + ((j & 1) ? C::TM_S1 : C::TM_S0) + ks * 8;
-            if constexpr (DT == kE4M3)
-              tc_mma_f8_ts(tmem + C::TM_O, a_t, v_desc, C::IDESC_PV, acc);
-            else
-              tc_mma_f16_ts(tmem + C::TM_O, a_t, v_desc, C::IDESC_PV, acc);
-          } else {
-            const uint32_t a_off =
-                (ks / C::KSTEPS_PER_PANEL) * C::PANEL + (ks % C::KSTEPS_PER_PANEL) * 32;
-            mma_issue<DT>(tmem + C::TM_O, smem_desc_sw128(p_addr + a_off, 16, 1024), v_desc,
-                          C::IDESC_PV, acc);
-          }
+          const uint32_t a_t = tmem + ((j & 1) ? C::TM_S1 : C::TM_S0) + ks * 8;
+          if constexpr (DT == kE4M3)
+            tc_mma_f8_ts(tmem + C::TM_O, a_t, v_desc, C::IDESC_PV, acc);
+          else
+            tc_mma_f16_ts(tmem + C::TM_O, a_t, v_desc, C::IDESC_PV, acc);
         }
         tc_commit(o_ready);
         tc_commit(v_empty + 8 * st);
@@ -367,7 +326,6 @@ __global__ void __launch_bounds__(192, 1)
     float sl2 = p.scale * 1.4426950408889634f;
     if (DT == kE4M3) sl2 *= __ldg(p.descale_q) * __ldg(p.descale_k);
     float m_run = -CUDART_INF_F, l_run = 0.f;
-    uint8_t* p_row = smem + C::OFF_P + r * 128;
     bool ok = true;
 
     for (int j = 0; j < nblk; ++j) {
@@ -453,44 +411,31 @@ __global__ void __launch_bounds__(192, 1)
         }
         l_run = l_run * alpha + rsum;
         m_run = m_new;
-        if constexpr (C::P_TMEM) {
-          // P over the first 64 columns of this block's S buffer (already read):
-          // column c holds keys 2c (low half) and 2c+1.
-          const uint32_t p_addr_t = tmem + lane_base + ((j & 1) ? C::TM_S1 : C::TM_S0);
-          if constexpr (DT == kE4M3) {
-            // e4m3: probabilities were produced pre-scaled by kP8Scale
+        // P over the first 64 columns of this block's S buffer (already read):
+        // column c holds keys 2c (low half) and 2c+1.
+        const uint32_t p_addr_t = tmem + lane_base + ((j & 1) ? C::TM_S1 : C::TM_S0);
+        if constexpr (DT == kE4M3) {
+          // e4m3: probabilities were produced pre-scaled by kP8Scale
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                make_float2(s[4 * c], s[4 * c + 1]), __NV_SATFINITE, __NV_E4M3);
+            const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                make_float2(s[4 * c + 2], s[4 * c + 3]), __NV_SATFINITE, __NV_E4M3);
+            pk[c] = (uint32_t)lo | ((uint32_t)hi << 16);
+          }
+          tmem_st32(p_addr_t, pk);
+        } else {
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
             uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-                  make_float2(s[4 * c], s[4 * c + 1]), __NV_SATFINITE, __NV_E4M3);
-              const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-                  make_float2(s[4 * c + 2], s[4 * c + 3]), __NV_SATFINITE, __NV_E4M3);
-              pk[c] = (uint32_t)lo | ((uint32_t)hi << 16);
-            }
-            tmem_st32(p_addr_t, pk);
-          } else {
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              uint32_t pk[32];
-#pragma unroll
-              for (int c = 0; c < 32; ++c) pk[c] = pack2(s[64 * h2 + 2 * c], s[64 * h2 + 2 * c + 1], DT);
-              tmem_st32(p_addr_t + 32 * h2, pk);
-            }
+            for (int c = 0; c < 32; ++c) pk[c] = pack2(s[64 * h2 + 2 * c], s[64 * h2 + 2 * c + 1], DT);
+            tmem_st32(p_addr_t + 32 * h2, pk);
           }
-          tmem_st_wait();
-        } else {
-          // P row, 128B-swizzled K-major: 16-byte chunk c of panel pp at
-          // position c ^ (r % 8).
-          constexpr int EPC = 16 / C::ES;  // P elements per 16-byte chunk
-#pragma unroll
-          for (int c = 0; c < 128 / EPC; ++c) {
-            const int pp = c / 8, cc = c % 8;
-            const uint4 w = pack_p16<DT>(s + c * EPC);
-            *reinterpret_cast<uint4*>(p_row + pp * C::PANEL + ((cc ^ (r & 7)) << 4)) = w;
-          }
-          fence_proxy_async_smem();
         }
+        tmem_st_wait();
       }
       tc_fence_before();
       mbar_arrive(p_ready);

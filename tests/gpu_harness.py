@@ -8,12 +8,17 @@ import torch
 
 import oracle
 import split_kv_flashattention_gb300 as fa
+from tolerance import excess
 
 # Tolerances: cutlass "Adds variable sequence lengths to the Hopper CuTe DSL
 # FMHA example", section "Tests" (fp16/bf16 atol 1e-2; fp8 atol 0.13,
-# rtol 1e-5); LSE atol 1e-3 for every dtype.
+# rtol 1e-5); LSE atol 1e-3 for every dtype.  They bound the value the
+# kernel computes; the stored 16-bit O is that value rounded to its type
+# (tests/tolerance.py).
 TOL = {"bf16": (1e-2, 0.0), "fp16": (1e-2, 0.0), "e4m3": (0.13, 1e-5)}
 LSE_ATOL = 1e-3
+# output type of each input type when the call leaves it to the library
+OUT_FMT = {"bf16": "bf16", "fp16": "fp16", "e4m3": "bf16"}
 
 
 def device():
@@ -91,8 +96,9 @@ def assert_close(inp, out, lse, o_ref, l_ref, heads=None):
         o_h = out[:tq, h]
         r_h = o_ref[:, h] if heads is None else o_ref[h]
         assert np.isfinite(o_h).all(), f"head {h}: non-finite or unwritten output"
-        err = np.abs(o_h - r_h) - (atol + rtol * np.abs(r_h))
-        assert err.max() <= 0, f"head {h}: max|dO|={np.abs(o_h - r_h).max():.4g}"
+        err = excess(o_h, r_h, atol, rtol, OUT_FMT[inp.dtype])
+        assert err.max() <= 0, (f"head {h}: max|dO|={np.abs(o_h - r_h).max():.4g}, "
+                                f"beyond the tolerance by {err.max():.3g}")
         if lse is not None:
             l_h = lse[h, :tq]
             lr = l_ref[h] if heads is None else l_ref[h]

@@ -38,6 +38,30 @@ def test_header_declares_the_expected_entry_points():
         assert s in syms
 
 
+# What a declaration's comment must name: one of the pages the library
+# follows, or the statement that the pages have no counterpart.
+PAGE_NAMES = ('flash-attention PR "[Cute,Fwd,Sm100] Support q_stage=1 for inference"',
+              'aiter PR "[FlyDSL] Enable FP8 FMHA split-K for short cached-prefix queries"',
+              'cutlass "Adds variable sequence lengths to the Hopper CuTe DSL FMHA example"')
+NO_COUNTERPART = ("no counterpart", "do not describe")
+
+
+def test_every_declaration_cites_a_page_or_says_it_has_none():
+    text = open(HEADER).read()
+    # the comment text between the previous declaration (or the top of the
+    # file's declarations) and each FA_API declaration, whitespace collapsed
+    decls = list(re.finditer(r"FA_API\s+[\w\s\*]+?\b(fa_\w+)\s*\(", text))
+    assert decls
+    prev_end = text.index("extern \"C\"")
+    for m in decls:
+        block = " ".join(text[prev_end:m.start()].replace("*", " ").split())
+        page = any(" ".join(p.split()) in block for p in PAGE_NAMES)
+        short = any(k in block for k in ('flash-attention PR', 'aiter PR', 'cutlass PR'))
+        none = any(k in block for k in NO_COUNTERPART)
+        assert page or short or none, f"{m.group(1)}: no page cited"
+        prev_end = text.index(";", m.end())
+
+
 def test_library_exports_every_declared_symbol(fa):
     lib = ctypes.CDLL(fa.LIB_PATH)
     for s in _declared_symbols():

@@ -197,7 +197,7 @@ def test_cuda_graph_replay_persistent_prefill():
     call's own stream order, so a captured call replays correctly: every
     replay claims the whole tile list again."""
     lens = [700, 300, 520]
-    inp = _quarter_v(make_inputs(lens, lens, 4, 2, 128, 128, "bf16", seed=46))
+    inp = (make_inputs(lens, lens, 4, 2, 128, 128, "bf16", seed=46))
     dev = torch.device("cuda:0")
     q, k, v, cq, ck, out, lse, ws = _prefill_buffers(inp, dev)
     s = torch.cuda.Stream()
@@ -227,7 +227,7 @@ def test_persistent_prefill_two_streams_own_workspaces():
     dev = torch.device("cuda:0")
     runs = []
     for seed, lens in ((47, [900, 260, 1100]), (48, [513, 2047, 64, 300])):
-        inp = _quarter_v(make_inputs(lens, lens, 8, 2, 128, 128, "bf16", seed=seed))
+        inp = (make_inputs(lens, lens, 8, 2, 128, 128, "bf16", seed=seed))
         bufs = _prefill_buffers(inp, dev)
         q, k, v, cq, ck, out, lse, ws = bufs
         fa.fa_fwd_splitkv_ex(q, k, v, cq, ck, inp.max_seqlen_q, out, lse, ws, num_splits=1)
@@ -271,7 +271,7 @@ def test_auto_kernel_choice():
     run_gpu(make_inputs([300], [300], 2, 2, 256, 256, "bf16", seed=51), num_splits=1)
     assert last() == fa.FA_KID_UMMA
     lens = [700, 300]
-    inp = _quarter_v(make_inputs(lens, lens, 4, 2, 128, 128, "bf16", seed=52))
+    inp = (make_inputs(lens, lens, 4, 2, 128, 128, "bf16", seed=52))
     for causal in (False, True):
         run_gpu(inp, causal=causal, num_splits=1)
         assert last() == fa.FA_KID_UMMA2_PERSISTENT
@@ -308,7 +308,7 @@ def test_persistent_prefill_random_shapes(seed):
     mask = str(rng.choice(["none", "causal", "window"]))
     causal = mask == "causal"
     wl = int(rng.integers(0, 300)) if mask == "window" else -1
-    inp = _quarter_v(make_inputs(lq, lk, group * h_kv, h_kv, d, d, dtype, seed=seed))
+    inp = (make_inputs(lq, lk, group * h_kv, h_kv, d, d, dtype, seed=seed))
     out, lse = run_gpu(inp, causal=causal, window_left=wl, num_splits=1, guard_rows=1)
     assert fa.fa_debug_last_kernel() == fa.FA_KID_UMMA2_PERSISTENT
     o_ref, l_ref = reference(inp, 0.0, causal, wl)
@@ -321,7 +321,7 @@ def test_persistent_prefill_large_groups(group, mask):
     """GQA groups of 16 to 128 query heads per KV head: a 128-row tile then
     holds 8, 4 or 1 queries, and a pair 16, 8 or 2."""
     lens_q, lens_k = [150, 37, 0, 90], [150, 60, 25, 90]
-    inp = _quarter_v(make_inputs(lens_q, lens_k, group, 1, 64, 64, "bf16", seed=54 + group))
+    inp = (make_inputs(lens_q, lens_k, group, 1, 64, 64, "bf16", seed=54 + group))
     causal = mask == "causal"
     wl = 40 if mask == "window" else -1
     out, lse = run_gpu(inp, causal=causal, window_left=wl, num_splits=1, guard_rows=1)
@@ -339,7 +339,7 @@ def test_persistent_capacity(lens, persistent):
     bounds the units by batch x pairs of the longest sequence.  With GQA 8:1 a
     pair is 32 queries: 128 x 32 = 4096 units fit, 128 x 33 = 4224 and 129
     sequences run the non-persistent kernel.  Results are correct either way."""
-    inp = _quarter_v(make_inputs(lens, lens, 16, 2, 64, 64, "bf16", seed=53))
+    inp = (make_inputs(lens, lens, 16, 2, 64, 64, "bf16", seed=53))
     out, lse = run_gpu(inp, causal=True, num_splits=1)
     assert fa.fa_debug_last_kernel() == (fa.FA_KID_UMMA2_PERSISTENT if persistent else fa.FA_KID_UMMA2)
     o_ref, l_ref = reference(inp, 0.0, True)
@@ -546,9 +546,6 @@ def test_running_max_jumps_between_blocks(kernel, growth, causal):
             if r0 < r1:
                 k[r0:r1] *= f
     inp.k = k.to(inp.k.dtype)
-    # Such peaked rows give O close to one V row; V / 4 keeps |O| < 1, where
-    # rounding O to bf16 costs under 2^-9 of the 1e-2 tolerance.
-    inp.v = (inp.v.float() * 0.25).to(inp.v.dtype)
     out, lse = run_gpu(inp, causal=causal, num_splits=1, flags=kernel)
     o_ref, l_ref = reference(inp, 0.0, causal)
     assert_close(inp, out, lse, o_ref, l_ref)
@@ -560,12 +557,6 @@ def test_running_max_jumps_between_blocks(kernel, growth, causal):
 # instantiation for calls with a causal or window mask, one without).  Its
 # arithmetic is the two-tile kernel's, so besides the oracle check its output
 # must equal that kernel's bit for bit.
-#
-# Rows that see only one or two keys make O a mix of very few V rows with
-# weights rounded to bf16 for the PV MMA; with O rounded to bf16 too, the
-# error bound is 2^-8 * max|V|, which passes the 1e-2 tolerance only while
-# max|V| < 2.56.  Tests whose subject is the tile walk scale V by 1/4; the
-# bound itself is checked in test_tensor_core_p_rounding_bound.
 
 @pytest.mark.parametrize("mask", ["none", "causal", "window"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
@@ -582,28 +573,29 @@ def test_persistent_prefill_edge_lengths(mask, dtype):
     assert np.array_equal(out, out2, equal_nan=True) and np.array_equal(lse, lse2, equal_nan=True)
 
 
-@pytest.mark.parametrize("mask", ["causal", "window"])
-def test_tensor_core_p_rounding_bound(mask):
-    """Edge lengths on another seed, where a causal row with two keys and
-    |V| near 4.5 puts the bf16 rounding of P and O at about 1.07e-2: the
-    error stays within 2^-8 * max|V| (P weights and O each rounded to bf16,
-    relative 2^-9), and LSE, which uses the fp32 row sums, within 1e-3."""
-    inp = workload("edge", dtype="bf16", seed=41)
+EDGE_SEEDS = [0, 1, 2, 3, 4, 5, 6, 7, 41, 53, 55]
+
+
+@pytest.mark.parametrize("seed", EDGE_SEEDS)
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("mask", ["none", "causal", "window"])
+def test_edge_lengths_raw_seeds(seed, dtype, mask):
+    """The edge workload (1, 0, 63, 64, 65, 128, 129, 700), GQA 8:2, raw
+    N(0,1) inputs, on many seeds and every kernel.  Causal rows that see one
+    or two keys make O a mix of very few V rows, weighted by probabilities
+    that the tensor-core kernels round to the 16-bit type for the PV MMA;
+    with |V| up to about 4.5 these are the rows that come closest to the
+    tolerance.  Seeds 2, 41, 53 and 55 are among the closest: on 55 the exact
+    result of one element, -4.1669, is itself 0.0107 from its nearest bf16
+    value, which is why the stored value is judged by the value it rounds
+    from (tests/tolerance.py)."""
+    inp = workload("edge", dtype=dtype, seed=seed)
     causal = mask == "causal"
     wl = 128 if mask == "window" else -1
-    out, lse = run_gpu(inp, causal=causal, window_left=wl, num_splits=1)
     o_ref, l_ref = reference(inp, 0.0, causal, wl)
-    tq = inp.q.shape[0]
-    bound = 2.0 ** -8 * float(inp.v.float().abs().max()) + 1e-4
-    assert np.abs(out[:tq] - o_ref).max() <= bound
-    fin = np.isfinite(l_ref)
-    assert np.array_equal(np.isneginf(lse[:, :tq]), np.isneginf(l_ref))
-    assert np.abs(lse[:, :tq][fin] - l_ref[fin]).max() <= 1e-3
-
-
-def _quarter_v(inp):
-    inp.v = (inp.v.float() * 0.25).to(inp.v.dtype)
-    return inp
+    for kernel in [fa.FA_KERNEL_AUTO] + KERNELS:
+        out, lse = run_gpu(inp, causal=causal, window_left=wl, flags=kernel)
+        assert_close(inp, out, lse, o_ref, l_ref)
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -611,7 +603,7 @@ def test_persistent_prefill_many_tiles(causal):
     """More (sequence, head, query pair) tiles than SMs, skewed lengths, d=64,
     GQA 8:1: every CTA walks several tiles of different sizes."""
     lens = [1500, 257, 0, 900, 64, 1, 700, 2048, 300, 513]
-    inp = _quarter_v(make_inputs(lens, lens, 16, 2, 64, 64, "bf16", seed=42))
+    inp = (make_inputs(lens, lens, 16, 2, 64, 64, "bf16", seed=42))
     out, lse = run_gpu(inp, causal=causal, num_splits=1)
     o_ref, l_ref = reference(inp, 0.0, causal)
     assert_close(inp, out, lse, o_ref, l_ref)
@@ -624,7 +616,7 @@ def test_persistent_prefill_q_and_k_lengths_differ(causal):
     """Lq != Lk (bottom-right causal: early query rows may see no key, so some
     tiles have no key block at all) and a sequence with queries but no keys."""
     lens_q, lens_k = [300, 129, 600, 40, 200], [100, 900, 600, 0, 450]
-    inp = _quarter_v(make_inputs(lens_q, lens_k, 8, 4, 128, 128, "bf16", seed=43))
+    inp = (make_inputs(lens_q, lens_k, 8, 4, 128, 128, "bf16", seed=43))
     out, lse = run_gpu(inp, causal=causal, num_splits=1)
     o_ref, l_ref = reference(inp, 0.0, causal)
     assert_close(inp, out, lse, o_ref, l_ref)
@@ -636,7 +628,7 @@ def test_persistent_prefill_out_not_32_byte_aligned(causal):
     starts 16 bytes past a 32-byte boundary takes the non-persistent two-tile
     kernel: same bits, and nothing written before O."""
     lens = [700, 300, 520]
-    inp = _quarter_v(make_inputs(lens, lens, 4, 2, 128, 128, "bf16", seed=45))
+    inp = (make_inputs(lens, lens, 4, 2, 128, 128, "bf16", seed=45))
     out, lse = run_gpu(inp, causal=causal, num_splits=1)
     o_ref, l_ref = reference(inp, 0.0, causal)
     assert_close(inp, out, lse, o_ref, l_ref)
@@ -653,7 +645,7 @@ def test_persistent_prefill_running_max_jumps(growth, causal):
     make that fallback run, with sums that overflow to inf in the extreme
     case."""
     lens = [700, 300, 520]
-    inp = _quarter_v(make_inputs(lens, lens, 2, 2, 128, 128, "bf16", seed=44))
+    inp = (make_inputs(lens, lens, 2, 2, 128, 128, "bf16", seed=44))
     factors = [1.0, 1.0, 8.0, 8.0, 40.0, 1.0] if growth == "moderate" else [1.0, 200.0, 1.0, 1.0, 1.0, 1.0]
     k = inp.k.float()
     cu = inp.cu_seqlens_k.tolist()
@@ -675,12 +667,9 @@ def test_persistent_prefill_running_max_jumps(growth, causal):
 def test_edge_lengths_gqa_matrix(kernel, h_kv, mask):
     """cutlass varlen page, "Tests": the edge lengths (1, 0, 63, 64, 65, 128,
     129, 700) x GQA 8:8, 8:2, 8:1 x no mask / causal / window (128, 0), on
-    every kernel (AUTO runs the persistent kernel without a mask). V / 2
-    keeps the bf16 rounding bound 2^-8 max|V| of rows with one or two keys
-    under the 1e-2 tolerance (see test_tensor_core_p_rounding_bound)."""
+    every kernel (AUTO runs the persistent kernel)."""
     lens = [1, 0, 63, 64, 65, 128, 129, 700]
     inp = make_inputs(lens, lens, 8, h_kv, 128, 128, "bf16", seed=45)
-    inp.v = (inp.v.float() * 0.5).to(inp.v.dtype)
     causal = mask == "causal"
     wl = 128 if mask == "window" else -1
     out, lse = run_gpu(inp, causal=causal, window_left=wl, num_splits=1, flags=kernel)

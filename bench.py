@@ -252,12 +252,14 @@ def config_fields(fa, dev, hbm_peak, tensor_peak):
     for prefix, spec, ns, kind in CONFIG_FIELDS:
         case = Case(fa, dev, spec, num_splits=ns)
         ms = med(graph_times(case, dev))
+        kern_tag = KERNEL_TAGS.get(fa.fa_debug_last_kernel(), "?")
         out[prefix + "_us"] = ms * 1e3
         if kind == "hbm":
             mb = metric_bytes(case.inp)
             out[prefix + "_tbs"] = mb / (ms * 1e-3) / 1e12
             out[prefix + "_frac"] = mb / (ms * 1e-3) / 1e9 / hbm_peak
             out[prefix + "_ns"] = case.ns
+            out[prefix + "_kernel"] = kern_tag
         elif kind == "tensor":
             tf = flops(case.inp, case.causal) / (ms * 1e-3) / 1e12
             out[prefix + "_tflops"] = tf
@@ -591,6 +593,7 @@ def main():
         raise RuntimeError("device error during warm-up")
     # the partial kernel the library chose (the last call above enqueued it)
     kern_tag = KERNEL_TAGS[fa.fa_debug_last_kernel()]
+    has_combine = ns > 1  # the split combine runs after the partial kernel
 
     # Timed region: exactly K steps (one library call each: partial kernel,
     # then the combine as its programmatic dependent when ns > 1), captured
@@ -601,7 +604,7 @@ def main():
     side.wait_stream(stream)
     graphs = {"step": graph_of(args.steps, 0),
               "partial": graph_of(args.steps, fa.FA_RUN_PARTIAL_ONLY)}
-    if ns > 1:
+    if has_combine:
         graphs["combine"] = graph_of(args.steps, fa.FA_RUN_COMBINE_ONLY)
 
     def replay(g):
@@ -627,7 +630,7 @@ def main():
     # The dominant (partial) kernel alone, K launches, for its roofline; then
     # the combine alone over the same workspace.
     partial_ms = replay(graphs["partial"]) / args.steps
-    combine_ms = replay(graphs["combine"]) / args.steps if ns > 1 else 0.0
+    combine_ms = replay(graphs["combine"]) / args.steps if has_combine else 0.0
     err = fa.fa_get_device_error(clear=True)
     if err != 0:
         raise RuntimeError(f"device error {fa.fa_status_string(err)}")
@@ -729,7 +732,7 @@ def main():
             "roofline": roof,
             "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps * (2 if ns > 1 else 1),
+            "gpu_launches": args.steps * (2 if has_combine else 1),
             "clocks": clocks,
         }
         if cfg is not None:

@@ -34,6 +34,27 @@ int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Order of the persistent prefill kernel's tile walk (both longest first).
+// Sequence-major: sequences by key count, each one's query pairs from the
+// last down, every KV head of a (sequence, pair) together; a sequence's key
+// prefix is then read by consecutive tiles while it is in L2.  m-major (a
+// masked call's option): every sequence's last pair first, level by level,
+// which revisits each (sequence, KV head) once per level; its KV heads can
+// be walked in groups whose K/V fits kHeadGroupBytes of L2.
+constexpr int kMaskedMmajor = 0;
+constexpr long long kHeadGroupBytes = 32ll << 20;
+void persistent_order(int h_kv, int total_k, int kv_row_elems, int es, bool masked,
+                      int* mmajor, int* head_group) {
+  *mmajor = masked && kMaskedMmajor;
+  *head_group = h_kv;
+  if (!*mmajor) return;
+  const long long per_head = (long long)total_k * kv_row_elems * es;
+  int best = 1;
+  for (int g = 1; g <= h_kv; ++g)
+    if (h_kv % g == 0 && (long long)g * per_head <= kHeadGroupBytes) best = g;
+  *head_group = best;
+}
+
 // The partial kernel the calling thread's last forward call launched
 // (fa_kernel_id), for fa_debug_last_kernel.
 thread_local int t_last_kernel = FA_KID_NONE;
@@ -481,6 +502,8 @@ int fwd_impl(const void* q, const void* k, const void* v, const int* cu_seqlens_
         const long long tiles = (long long)batch * pairs * h_kv;
         dim3 grid((unsigned)(tiles < sms ? tiles : sms), 1, 1);
         p.sched = static_cast<int*>(workspace);
+        persistent_order(h_kv, total_k, d_qk + d_v, es, p.causal || p.window_left >= 0,
+                         &p.unit_mmajor, &p.kv_head_group);
         if (cudaMemsetAsync(p.sched, 0, sizeof(int), s) != cudaSuccess) return FA_ERR_CUDA;
         e = in_dtype == kFP16 ? launch_umma2p_fp16(d_qk, d_v, p, tmQ, tmK, tmV, grid, s)
                               : launch_umma2p_bf16(d_qk, d_v, p, tmQ, tmK, tmV, grid, s);

@@ -64,6 +64,8 @@ struct FwdParams {
   int page_shift;   // log2(page_size)
   int num_sms;      // SMs of the device (0 if unknown)
   int* sched;       // persistent kernel's tile ticket counter, zero at launch
+  int kv_head_group;  // persistent kernel: KV heads per group of its tile walk (divides h_kv)
+  int unit_mmajor;    // persistent kernel: units m-major (1) or by key count, last pair first (0)
 };
 
 struct SeqInfo {

@@ -190,4 +190,48 @@ __device__ __forceinline__ void store_o(void* out, size_t elem, const float* f, 
   }
 }
 
+// Output row of one warp (lane l holds columns [l*DPL, (l+1)*DPL)) written
+// with 16-byte stores.  W packed 32-bit words per lane; the first lane of
+// every group of 4/W lanes collects the group's 16 bytes.  The row starts
+// on a 16-byte boundary (O is 16-byte aligned, rows are d_v elements).
+template <int W>
+__device__ __forceinline__ void store_row_16B(uint8_t* row, int lane, const uint32_t* w) {
+  constexpr int G = 4 / W;
+  uint32_t v[4];
+#pragma unroll
+  for (int i = 0; i < W; ++i) v[i] = w[i];
+#pragma unroll
+  for (int g = 1; g < G; ++g)
+#pragma unroll
+    for (int i = 0; i < W; ++i) v[g * W + i] = __shfl_down_sync(0xffffffffu, w[i], g);
+  if ((lane & (G - 1)) == 0)
+    *reinterpret_cast<uint4*>(row + lane * W * 4) = make_uint4(v[0], v[1], v[2], v[3]);
+}
+
+template <int DPL>
+__device__ __forceinline__ void store_combined_row(void* out, size_t row_elem, const float* f,
+                                                   int lane, int out_dtype) {
+  if (out_dtype == kE4M3) {
+    if constexpr (DPL % 4 == 0) {
+      uint32_t w[DPL / 4];
+#pragma unroll
+      for (int i = 0; i < DPL / 4; ++i) {
+        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+            make_float2(f[4 * i], f[4 * i + 1]), __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+            make_float2(f[4 * i + 2], f[4 * i + 3]), __NV_SATFINITE, __NV_E4M3);
+        w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+      }
+      store_row_16B<DPL / 4>(static_cast<uint8_t*>(out) + row_elem, lane, w);
+    } else {
+      store_o<DPL>(out, row_elem + lane * DPL, f, 1.f, out_dtype);
+    }
+  } else {
+    uint32_t w[DPL / 2];
+#pragma unroll
+    for (int i = 0; i < DPL / 2; ++i) w[i] = pack2(f[2 * i], f[2 * i + 1], out_dtype);
+    store_row_16B<DPL / 2>(static_cast<uint8_t*>(out) + row_elem * 2, lane, w);
+  }
+}
+
 }  // namespace fa

@@ -89,10 +89,18 @@ struct PTile {
 };
 static_assert(sizeof(PTile) <= 64, "tile ring slot");
 
+// Tile r of the walk: KV heads in groups of p.kv_head_group; within a group
+// the unit list in order, the group's heads innermost.  One group (all
+// heads) without a mask; under a mask the host sizes a group so that its K/V
+// stays in L2 while the m-major list revisits each sequence's key prefix.
 __device__ __forceinline__ void decode_ptile(const FwdParams& p, const uint16_t* units, int r,
-                                             int qpt, PTile& t) {
-  const int u = units[r / p.h_kv];
-  t.kh = r - (r / p.h_kv) * p.h_kv;
+                                             int n_units, int qpt, PTile& t) {
+  const int hg = p.kv_head_group;
+  const int per_group = n_units * hg;
+  const int g = r / per_group;
+  const int rem = r - g * per_group;
+  const int u = units[rem / hg];
+  t.kh = g * hg + (rem - (rem / hg) * hg);
   t.b = u & 127;
   t.m_blk = u >> 7;
   load_seq(p, t.b, t.sq);  // validated when the list was built
@@ -207,8 +215,7 @@ __global__ void __launch_bounds__(384, 1)
       s_keys[bb] = key;
     }
     __syncthreads();
-    const bool masked = p.causal || p.window_left >= 0;
-    if (!masked) {
+    if (!p.unit_mmajor) {
       // sequences by key count, longest first (ties by index)
       for (int bb = lt; bb >= 0 && bb < p.batch; bb += blockDim.x - 128) {
         int rk = 0;
@@ -261,7 +268,8 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();  // also publishes the tile list (and frees the scratch)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int n_tiles = *n_units_s * p.h_kv;
+  const int n_units = *n_units_s;
+  const int n_tiles = n_units * p.h_kv;
 
   if (warp < 4) {
     regs_dec<CP::REGS_CTRL>();
@@ -327,7 +335,7 @@ __global__ void __launch_bounds__(384, 1)
           const int r = claimed;
           PTile T = {};
           if (r >= 0)
-            decode_ptile(p, units, r, qpt, T);
+            decode_ptile(p, units, r, n_units, qpt, T);
           else
             T.b = -1;
           // hand the decoded tile (or the end mark) to the MMA and softmax roles
@@ -371,7 +379,7 @@ __global__ void __launch_bounds__(384, 1)
           claimed = ticket_tile(atomicAdd(p.sched, 1), n_tiles);
           if (claimed >= 0) {
             PTile T2;
-            decode_ptile(p, units, claimed, qpt, T2);
+            decode_ptile(p, units, claimed, n_units, qpt, T2);
             if (T2.nblk > 0) prefetch_tile(T2);
           }
         }

@@ -728,3 +728,51 @@ def test_fp8_output_saturates():
         big = np.abs(o_ref) > 480.0
         assert big.any() and np.array_equal(np.sign(out[:tq][big]), np.sign(o_ref[big]))
         assert np.all(np.abs(out[:tq][big]) == 448.0)
+
+
+# ------------------------------------------------ one-tile kernel, splits
+# The one-tile tensor-core kernel with 2 to 8 splits: splits that see no key
+# (short sequences, early causal rows), tiles with fewer rows than splits, a
+# null LSE pointer, e4m3 output and each input type, against the oracle.
+
+@pytest.mark.parametrize("ns", [2, 3, 4, 5, 6, 7, 8])
+def test_one_tile_split_counts(ns):
+    lens_k = [3000, 17, 0, 1, 999, 4100]
+    inp = make_inputs([1] * 6, lens_k, 16, 4, 128, 128, "bf16", seed=60 + ns)
+    out, lse = run_gpu(inp, num_splits=ns, flags=fa.FA_KERNEL_UMMA, ws_guard=16)
+    assert fa.fa_debug_last_kernel() == fa.FA_KID_UMMA
+    o_ref, l_ref = reference(inp)
+    assert_close(inp, out, lse, o_ref, l_ref)
+    assert np.all(out[2] == 0) and np.all(np.isneginf(lse[:, 2]))
+
+
+@pytest.mark.parametrize("dtype,d_qk,d_v", [("bf16", 64, 64), ("fp16", 64, 64), ("fp16", 128, 128),
+                                            ("e4m3", 192, 128), ("e4m3", 128, 128)])
+@pytest.mark.parametrize("mask", ["none", "causal", "window"])
+def test_one_tile_prefix_masks(dtype, d_qk, d_v, mask):
+    """Short prefixes (Lq = 70, 3, 33) against longer key sequences, split 8
+    and 5 ways: under a causal or window mask early rows see few keys, so
+    some splits of a row are empty, and a 3-row sequence's tile has fewer
+    rows than splits."""
+    inp = make_inputs([70, 3, 33], [1500, 40, 900], 6, 3, d_qk, d_v, dtype, seed=71)
+    causal = mask == "causal"
+    wl = 128 if mask == "window" else -1
+    for ns in (8, 5):
+        out, lse = run_gpu(inp, causal=causal, window_left=wl, num_splits=ns,
+                           flags=fa.FA_KERNEL_UMMA)
+        o_ref, l_ref = reference(inp, 0.0, causal, wl)
+        assert_close(inp, out, lse, o_ref, l_ref)
+
+
+def test_fp8_prefix_null_lse_and_fp8_output():
+    """The FP8 cached prefix at 4096 keys through AUTO, with and without an
+    LSE output, and with e4m3 O."""
+    inp = workload("fp8_prefix", kv=4096)
+    o_ref, l_ref = reference(inp)
+    out, lse = run_gpu(inp)
+    assert fa.fa_debug_last_kernel() == fa.FA_KID_UMMA
+    assert_close(inp, out, lse, o_ref, l_ref)
+    out2, lse2 = run_gpu(inp, with_lse=False)
+    assert lse2 is None and np.array_equal(out, out2)
+    out3, lse3 = run_gpu(inp, out_dtype=torch.float8_e4m3fn)
+    _assert_close_e4m3_out(inp, out3, lse3, o_ref, l_ref)

@@ -72,7 +72,9 @@ typedef enum {
   FA_ERR_WORKSPACE = -3,      /* workspace missing or too small            */
   FA_ERR_CUDA = -4,           /* a CUDA runtime call failed                */
   FA_ERR_DEVICE_TIMEOUT = -5, /* device: a pipeline wait ran out of time   */
-  FA_ERR_DEVICE_ARG = -6      /* device: cu_seqlens inconsistent with sizes */
+  FA_ERR_DEVICE_ARG = -6,     /* device: cu_seqlens inconsistent with sizes */
+  FA_ERR_DEVICE_BOUNDS = -7   /* device, debug build only: an index failed its
+                                 bounds check and the access was skipped     */
 } fa_status;
 
 /* Kernel selection (flags argument of fa_fwd_splitkv_ex). */

@@ -29,6 +29,10 @@ __all__ = [
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libfa_splitkv.so")
+# the bounds-checking build (python -m split_kv_flashattention_gb300.build --debug),
+# loaded instead when the environment variable FA_SPLITKV_DEBUG is 1
+LIB_DEBUG_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib",
+                              "libfa_splitkv_debug.so")
 
 FA_KERNEL_AUTO, FA_KERNEL_SIMT, FA_KERNEL_UMMA, FA_KERNEL_UMMA2 = 0, 1, 2, 3
 FA_RUN_PARTIAL_ONLY, FA_RUN_COMBINE_ONLY = 4, 8
@@ -63,10 +67,13 @@ def library() -> ctypes.CDLL:
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH):
+    debug = os.environ.get("FA_SPLITKV_DEBUG") == "1"
+    path = LIB_DEBUG_PATH if debug else LIB_PATH
+    if not os.path.exists(path):
         raise FaLibraryMissing(
-            f"{LIB_PATH} is missing; build it with python -m split_kv_flashattention_gb300.build")
-    lib = ctypes.CDLL(LIB_PATH)
+            f"{path} is missing; build it with python -m split_kv_flashattention_gb300.build"
+            + (" --debug" if debug else ""))
+    lib = ctypes.CDLL(path)
     lib.fa_fwd_splitkv_ex.restype = _c_int
     lib.fa_fwd_splitkv_ex.argtypes = [
         _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,

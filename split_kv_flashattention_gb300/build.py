@@ -4,6 +4,12 @@ Every translation unit under csrc/ is compiled in parallel to an object file
 under _build/, then linked into split_kv_flashattention_gb300/lib/
 libfa_splitkv.so with the CUDA runtime linked statically and only the fa_*
 C symbols exported.  Usage: python -m split_kv_flashattention_gb300.build
+
+--debug builds lib/libfa_splitkv_debug.so from the same sources with
+-DFA_DEBUG (objects under _build_debug/): every global index the kernels
+use is checked first, and a failed check records FA_ERR_DEVICE_BOUNDS in the
+device error word and skips the access.  The binding loads it when the
+environment variable FA_SPLITKV_DEBUG is 1.
 """
 
 from __future__ import annotations
@@ -21,6 +27,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libfa_splitkv.so")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(LIBDIR, "libfa_splitkv_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -45,12 +53,13 @@ def _headers():
         os.path.join(ROOT, "include", "fa_splitkv.h")]
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, verbose_ptxas: bool, debug: bool = False) -> str:
+    obj = os.path.join(BUILD_DEBUG if debug else BUILD, os.path.basename(src)[:-3] + ".o")
     newest_dep = max(os.path.getmtime(h) for h in _headers() + [src])
     if os.path.exists(obj) and os.path.getmtime(obj) >= newest_dep and not verbose_ptxas:
         return obj
-    cmd = [nvcc()] + _flags(["-Xptxas", "-v"] if verbose_ptxas else []) + ["-c", src, "-o", obj]
+    extra = (["-Xptxas", "-v"] if verbose_ptxas else []) + (["-DFA_DEBUG"] if debug else [])
+    cmd = [nvcc()] + _flags(extra) + ["-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -59,42 +68,47 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def _machine_stamp():
-    """Objects built on another host architecture are discarded."""
-    stamp = os.path.join(BUILD, "host_arch.txt")
+def _machine_stamp(build_dir: str = BUILD, lib: str = LIB):
+    """Objects (and the library) built on another host architecture are
+    discarded."""
+    stamp = os.path.join(build_dir, "host_arch.txt")
     arch = platform.machine()
     old = open(stamp).read().strip() if os.path.exists(stamp) else None
     if old != arch:
-        for d in (BUILD, LIBDIR):
-            for f in os.listdir(d):
-                if f.endswith((".o", ".so", ".tmp", ".map")):
-                    os.remove(os.path.join(d, f))
+        for f in os.listdir(build_dir):
+            if f.endswith((".o", ".tmp", ".map")):
+                os.remove(os.path.join(build_dir, f))
+        for f in (lib, lib + ".tmp"):
+            if os.path.exists(f):
+                os.remove(f)
         with open(stamp, "w") as f:
             f.write(arch + "\n")
 
 
-def build(verbose_ptxas: bool = False, jobs: int | None = None) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose_ptxas: bool = False, jobs: int | None = None, debug: bool = False) -> str:
+    build_dir = BUILD_DEBUG if debug else BUILD
+    lib = LIB_DEBUG if debug else LIB
+    os.makedirs(build_dir, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
-    _machine_stamp()
+    _machine_stamp(build_dir, lib)
     srcs = _sources()
     jobs = jobs or min(len(srcs), os.cpu_count() or 4)
     with cf.ThreadPoolExecutor(max_workers=jobs) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
-    vers = os.path.join(BUILD, "exports.map")
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, debug), srcs))
+    vers = os.path.join(build_dir, "exports.map")
     with open(vers, "w") as f:
         f.write("{ global: fa_*; local: *; };\n")
-    if os.path.exists(LIB) and os.path.getmtime(LIB) >= max(os.path.getmtime(o) for o in objs):
-        return LIB
-    tmp = LIB + ".tmp"
+    if os.path.exists(lib) and os.path.getmtime(lib) >= max(os.path.getmtime(o) for o in objs):
+        return lib
+    tmp = lib + ".tmp"
     cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + [
         "-Xlinker", f"--version-script={vers}", "-Xlinker", "--exclude-libs,ALL"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose_ptxas="-v" in sys.argv))
+    print(build(verbose_ptxas="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -275,6 +275,7 @@ const char* fa_status_string(int status) {
     case FA_ERR_CUDA: return "FA_ERR_CUDA";
     case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
     case FA_ERR_DEVICE_ARG: return "FA_ERR_DEVICE_ARG";
+    case FA_ERR_DEVICE_BOUNDS: return "FA_ERR_DEVICE_BOUNDS";
   }
   return "FA_UNKNOWN_STATUS";
 }

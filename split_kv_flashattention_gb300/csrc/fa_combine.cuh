@@ -57,6 +57,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ Fw
   // written as O = 0, LSE = -inf, so every split below ns is readable.
   auto load_o = [&](int s, float* v) {
     const float* src = obase + (size_t)s * ostride;
+    if (!ws_o_ok(p, (size_t)(src - p.ws_o), DPL)) src = p.ws_o;
     if constexpr (DPL % 4 == 0) {
 #pragma unroll
       for (int e = 0; e < DPL; e += 4) {
@@ -83,7 +84,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ Fw
 #pragma unroll
   for (int u = 0; u < kMaxSplits / 32; ++u) {
     const int s = u * 32 + lane;
-    lv[u] = s < ns ? __ldg(p.ws_l + s * split_stride + row0) : -CUDART_INF_F;
+    lv[u] = s < ns && ws_l_ok(p, s * split_stride + row0) ? __ldg(p.ws_l + s * split_stride + row0)
+                                                          : -CUDART_INF_F;
   }
 
   constexpr float kLog2e = 1.4426950408889634f;
@@ -135,8 +137,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ Fw
   }
 
   if (__any_sync(0xffffffffu, timed_out)) return;
-  store_combined_row<DPL>(p.out, ((size_t)t * p.h_q + h) * DV, acc, lane, p.out_dtype);
-  if (p.lse != nullptr && lane == 0) p.lse[(size_t)h * p.total_q + t] = lse_out;
+  if (o_ok(p, ((size_t)t * p.h_q + h) * DV, DV))  // warp-uniform
+    store_combined_row<DPL>(p.out, ((size_t)t * p.h_q + h) * DV, acc, lane, p.out_dtype);
+  if (p.lse != nullptr && lane == 0 && lse_ok(p, h, t)) p.lse[(size_t)h * p.total_q + t] = lse_out;
 }
 
 // Test hook: one thread waits, through the kernels' own bounded wait, on an

@@ -11,6 +11,8 @@
 
 #include <stdint.h>
 
+#include "fa_ptx.cuh"
+
 namespace fa {
 
 constexpr int kBlockN = 128;    // keys per split block
@@ -72,10 +74,50 @@ struct SeqInfo {
   int q0, lq, k0, lk;
 };
 
+// ---- bounds checks of the debug build (FA_DEBUG)
+// Every global access of the kernels goes through one of these predicates.
+// In a debug build a failed check records FA_ERR_DEVICE_BOUNDS in the error
+// word and the caller skips the access; the context stays usable.  In the
+// normal build they are constant true and compile away.
+#ifdef FA_DEBUG
+__device__ __forceinline__ bool dbg_ok(const FwdParams& p, bool ok) {
+  if (!ok) record_error(p.err, kErrDeviceBounds);
+  return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool dbg_ok(const FwdParams&, bool) { return true; }
+#endif
+// n elements of O from element `elem` on
+__device__ __forceinline__ bool o_ok(const FwdParams& p, size_t elem, int n) {
+  return dbg_ok(p, elem + n <= (size_t)p.total_q * p.h_q * p.d_v);
+}
+__device__ __forceinline__ bool lse_ok(const FwdParams& p, int h, int t) {
+  return dbg_ok(p, h >= 0 && h < p.h_q && t >= 0 && t < p.total_q);
+}
+// n fp32 partials of O from index `idx` on; one partial LSE at `idx`
+__device__ __forceinline__ bool ws_o_ok(const FwdParams& p, size_t idx, int n) {
+  return dbg_ok(p, p.ws_o != nullptr &&
+                       idx + n <= (size_t)p.num_splits * p.slots * p.h_q * p.d_v);
+}
+__device__ __forceinline__ bool ws_l_ok(const FwdParams& p, size_t idx) {
+  return dbg_ok(p, p.ws_l != nullptr && idx < (size_t)p.num_splits * p.slots * p.h_q);
+}
+// first row of a K/V or Q box (a box may run past the last row: TMA fills zeros)
+__device__ __forceinline__ bool kv_row_ok(const FwdParams& p, int row) {
+  return dbg_ok(p, row >= 0 && row < p.total_k);
+}
+__device__ __forceinline__ bool q_row_ok(const FwdParams& p, int row) {
+  return dbg_ok(p, row >= 0 && row < p.total_q);
+}
+__device__ __forceinline__ bool seq_ok_idx(const FwdParams& p, int b) {
+  return dbg_ok(p, b >= 0 && b < p.batch);
+}
+
 // Reads and validates one sequence's offsets.  A sequence whose lengths are
 // negative, exceed max_seqlen_q, or overrun the declared buffers is skipped
 // and reported through the error word (never read or written out of range).
 __device__ __forceinline__ bool load_seq(const FwdParams& p, int b, SeqInfo& s) {
+  if (!seq_ok_idx(p, b)) b = 0;
   s.q0 = __ldg(p.cu_q + b);
   s.lq = __ldg(p.cu_q + b + 1) - s.q0;
   if (p.page_size > 0) {
@@ -130,10 +172,15 @@ __device__ __forceinline__ void page_enter(const FwdParams& p, const SeqInfo& s,
 
 __device__ __forceinline__ int kv_row_walk(const FwdParams& p, const SeqInfo& s, int b, int key,
                                            int box, PageCursor& pc) {
-  if (p.page_size <= 0) return s.k0 + key;
-  if (key >= s.lk) key = (s.lk - 1) & ~(box - 1);
-  if (__builtin_expect(key < pc.lo || key >= pc.hi, 0)) page_enter(p, s, b, key, pc);
-  return pc.base + key;
+  int row;
+  if (p.page_size <= 0) {
+    row = s.k0 + key;
+  } else {
+    if (key >= s.lk) key = (s.lk - 1) & ~(box - 1);
+    if (__builtin_expect(key < pc.lo || key >= pc.hi, 0)) page_enter(p, s, b, key, pc);
+    row = pc.base + key;
+  }
+  return kv_row_ok(p, row) ? row : 0;
 }
 
 // ---- longest-first dispatch of decode tiles

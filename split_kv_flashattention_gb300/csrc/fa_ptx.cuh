@@ -20,6 +20,7 @@ namespace fa {
 // Error codes written to the device error word (match fa_status values).
 constexpr int kErrDeviceTimeout = -5;
 constexpr int kErrDeviceArg = -6;
+constexpr int kErrDeviceBounds = -7;  // debug builds: an index failed its bounds check
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -387,15 +387,19 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     const int h = kh * p.group + (R - i * p.group);
     const int t = sq.q0 + i;
     if (p.num_splits == 1) {
-      store_o<C::DPL>(p.out, ((size_t)t * p.h_q + h) * DV + lane * C::DPL, o, 1.f, p.out_dtype);
-      if (p.lse != nullptr && lane == 0) p.lse[(size_t)h * p.total_q + t] = lse_v;
+      const size_t oe = ((size_t)t * p.h_q + h) * DV + lane * C::DPL;
+      if (o_ok(p, oe, C::DPL)) store_o<C::DPL>(p.out, oe, o, 1.f, p.out_dtype);
+      if (p.lse != nullptr && lane == 0 && lse_ok(p, h, t)) p.lse[(size_t)h * p.total_q + t] = lse_v;
     } else {
       const size_t slot = (size_t)b * p.max_seqlen_q + i;
       const size_t row = ((size_t)split * p.slots + slot) * p.h_q + h;
-      float* wo = p.ws_o + row * DV + lane * C::DPL;
+      if (ws_o_ok(p, row * DV + lane * C::DPL, C::DPL)) {
+        float* wo = p.ws_o + row * DV + lane * C::DPL;
 #pragma unroll
-      for (int e = 0; e < C::DPL; e += 2) *reinterpret_cast<float2*>(wo + e) = make_float2(o[e], o[e + 1]);
-      if (lane == 0) p.ws_l[row] = lse_v;
+        for (int e = 0; e < C::DPL; e += 2)
+          *reinterpret_cast<float2*>(wo + e) = make_float2(o[e], o[e + 1]);
+      }
+      if (lane == 0 && ws_l_ok(p, row)) p.ws_l[row] = lse_v;
     }
   }
 

@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
       for (int pq = 0; pq < C::NPQ; ++pq)
         tma_load_3d(sbase + C::OFF_Q + pq * C::PANEL, &tmQ, q_full, pq * C::PANEL_ELEMS,
-                    kh * group, sq.q0 + q_start, pol_q);
+                    kh * group, q_row_ok(p, sq.q0 + q_start) ? sq.q0 + q_start : 0, pol_q);
       // K(0), K(1), V(0), K(2), V(1), ...: K one block ahead of V.
       PageCursor pages_k, pages_v;
       for (int j = 0; j <= nblk; ++j) {
@@ -471,21 +471,26 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(o[e]) * inv;
         if (p.num_splits == 1) {
-          store_o<32>(p.out, ((size_t)t * p.h_q + h) * DV + c * 32, f, 1.f, p.out_dtype);
+          const size_t oe = ((size_t)t * p.h_q + h) * DV + c * 32;
+          if (o_ok(p, oe, 32)) store_o<32>(p.out, oe, f, 1.f, p.out_dtype);
         } else {
           const size_t slot = (size_t)b * p.max_seqlen_q + i;
-          float4* dst = reinterpret_cast<float4*>(
-              p.ws_o + (((size_t)split * p.slots + slot) * p.h_q + h) * DV + c * 32);
+          const size_t we = (((size_t)split * p.slots + slot) * p.h_q + h) * DV + c * 32;
+          if (ws_o_ok(p, we, 32)) {
+            float4* dst = reinterpret_cast<float4*>(p.ws_o + we);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) dst[e] = make_float4(f[4 * e], f[4 * e + 1], f[4 * e + 2], f[4 * e + 3]);
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_float4(f[4 * e], f[4 * e + 1], f[4 * e + 2], f[4 * e + 3]);
+          }
         }
       }
       if (row_ok) {
         if (p.num_splits == 1) {
-          if (p.lse != nullptr) p.lse[(size_t)h * p.total_q + t] = lse_v;
+          if (p.lse != nullptr && lse_ok(p, h, t)) p.lse[(size_t)h * p.total_q + t] = lse_v;
         } else {
           const size_t slot = (size_t)b * p.max_seqlen_q + i;
-          p.ws_l[((size_t)split * p.slots + slot) * p.h_q + h] = lse_v;
+          const size_t wl = ((size_t)split * p.slots + slot) * p.h_q + h;
+          if (ws_l_ok(p, wl)) p.ws_l[wl] = lse_v;
         }
       }
     }

@@ -292,7 +292,8 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int pk = 0; pk < C::NPQ; ++pk)
             tma_load_3d(dst + pk * C::PANEL, &tmK, k_full + 8 * st, pk * C::PANEL_ELEMS, T.kh,
-                        T.sq.k0 + T.kb0 + j * kBlockN, pol_kv);
+                        kv_row_ok(p, T.sq.k0 + T.kb0 + j * kBlockN) ? T.sq.k0 + T.kb0 + j * kBlockN : 0,
+                        pol_kv);
           ++issued_k;
           return true;
         };
@@ -306,7 +307,8 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int pv = 0; pv < C::NPV; ++pv)
             tma_load_3d(dst + pv * C::PANEL, &tmV, v_full + 8 * st, pv * C::PANEL_ELEMS, T.kh,
-                        T.sq.k0 + T.kb0 + j * kBlockN, pol_kv);
+                        kv_row_ok(p, T.sq.k0 + T.kb0 + j * kBlockN) ? T.sq.k0 + T.kb0 + j * kBlockN : 0,
+                        pol_kv);
           ++issued_v;
           return true;
         };
@@ -360,7 +362,9 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int pq = 0; pq < C::NPQ; ++pq)
               tma_load_3d(sbase + C::OFF_Q + (t * C::NPQ + pq) * C::PANEL, &tmQ, q_full,
-                          pq * C::PANEL_ELEMS, T.kh * group, T.sq.q0 + T.q_start + t * qpt, pol_q);
+                          pq * C::PANEL_ELEMS, T.kh * group,
+                          q_row_ok(p, T.sq.q0 + T.q_start + t * qpt) ? T.sq.q0 + T.q_start + t * qpt : 0,
+                          pol_q);
           ++issued_q;
           // K(1), V(0), K(2), V(1), ...: K one block ahead of V.
           for (int j = 1; j <= T.nblk; ++j) {
@@ -709,11 +713,15 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (warp_active && row_ok) {
 #pragma unroll
-        for (int c = 0; c < DV / 32; ++c)
-          store_o<32, true>(p.out, ((size_t)tok * p.h_q + h) * DV + c * 32,
-                            reinterpret_cast<const float*>(o + 32 * c), inv, p.out_dtype);
+        for (int c = 0; c < DV / 32; ++c) {
+          const size_t oe = ((size_t)tok * p.h_q + h) * DV + c * 32;
+          if (o_ok(p, oe, 32))
+            store_o<32, true>(p.out, oe, reinterpret_cast<const float*>(o + 32 * c), inv,
+                              p.out_dtype);
+        }
       }
-      if (warp_active && row_ok && p.lse != nullptr) p.lse[(size_t)h * p.total_q + tok] = lse_v;
+      if (warp_active && row_ok && p.lse != nullptr && lse_ok(p, h, tok))
+        p.lse[(size_t)h * p.total_q + tok] = lse_v;
     }
     // teardown (softmax side): the TMEM release waits for these warps
     tc_fence_before();

@@ -74,6 +74,7 @@ def test_status_strings(fa):
     assert fa.fa_status_string(-1) == "FA_ERR_INVALID_ARG"
     assert fa.fa_status_string(-3) == "FA_ERR_WORKSPACE"
     assert fa.fa_status_string(-5) == "FA_ERR_DEVICE_TIMEOUT"
+    assert fa.fa_status_string(-7) == "FA_ERR_DEVICE_BOUNDS"
     assert fa.fa_status_string(12345) == "FA_UNKNOWN_STATUS"
 
 

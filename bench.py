@@ -328,6 +328,8 @@ def parse():
                     help="skip the per-configuration fields of the default line")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--kv", type=int, default=0, help="override the key length (long_decode)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the batch (gqa_decode, paged_decode): a smaller case for ncu")
     return ap.parse_args()
 
 
@@ -559,6 +561,8 @@ def main():
     kernel_flag = {"auto": fa.FA_KERNEL_AUTO, "simt": fa.FA_KERNEL_SIMT,
                    "umma": fa.FA_KERNEL_UMMA, "umma2": fa.FA_KERNEL_UMMA2}[args.kernel]
     kw = {"kv": args.kv} if args.kv else {}
+    if args.batch:
+        kw["batch"] = args.batch
     paged = spec.get("paged", 0)
     case = Case(fa, dev, spec, num_splits=args.num_splits, flags=kernel_flag, rotate=not paged,
                 kw_extra=kw)
@@ -684,7 +688,8 @@ def main():
     tpeak, _, tpeak_src = measured_tensor_peak()
     cfg = None
     t_cfg0 = t_cfg1 = None
-    if world == 1 and not args.no_configs and args.workload == "long_decode" and not args.kv:
+    if world == 1 and not args.no_configs and args.workload == "long_decode" and not args.kv \
+            and not args.batch:
         t_cfg0 = time.time()
         cfg = config_fields(fa, dev, peak_gbs, tpeak)
         t_cfg1 = time.time()

@@ -479,6 +479,7 @@ __global__ void __launch_bounds__(384, 1)
           for (int j = 0; ok && j < T.nblk; ++j) {
             const int vst = gv % VS;
             const bool last = j + 1 == T.nblk;
+            uint32_t s0m = 0;  // slots given the next tile's S(0)
             for (int t = 0; t < ntiles; ++t) {
               ok = mbar_wait(p_ready + 8 * t, (pcb >> t) & 1, p.err, abort_flag);
               pcb ^= 1u << t;
@@ -502,12 +503,22 @@ __global__ void __launch_bounds__(384, 1)
                   if (!ok) break;
                   n_ntiles = (N.b >= 0 && N.nblk > 0) ? (N.nq_b > 0 ? 2 : 1) : 0;
                 }
-                if (t < n_ntiles && !(ok = issue_s0(t))) break;
+                // the next tile's S(0) into every free slot up to this one
+                for (int u = 0; ok && u <= t && u < n_ntiles; ++u)
+                  if (!((s0m >> u) & 1)) {
+                    ok = issue_s0(u);
+                    s0m |= 1u << u;
+                  }
+                if (!ok) break;
               }
             }
             if (!ok) break;
             if (last)  // a slot this tile left idle
-              for (int t = ntiles; ok && t < n_ntiles; ++t) ok = issue_s0(t);
+              for (int t = 0; ok && t < n_ntiles; ++t)
+                if (!((s0m >> t) & 1)) {
+                  ok = issue_s0(t);
+                  s0m |= 1u << t;
+                }
             if (!ok) break;
             tc_commit(v_empty + 8 * vst);
             ++gv;

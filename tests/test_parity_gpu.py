@@ -622,6 +622,28 @@ def test_persistent_prefill_q_and_k_lengths_differ(causal):
     assert_close(inp, out, lse, o_ref, l_ref)
 
 
+@pytest.mark.parametrize("mask", ["causal", "window"])
+@pytest.mark.parametrize("shift", [0, 64, 200, -100])
+def test_persistent_prefill_mha_pair_last_block(mask, shift):
+    """MHA: a tile holds 128 queries, so under a causal or window mask the
+    first tile of a query pair can end a whole key block before the second;
+    its rows then see nothing of the pair's last block.  Lk = Lq + shift
+    moves the diagonal against the block grid.  The result equals the oracle
+    and, bit for bit, the non-persistent two-tile kernel."""
+    lens_q = [1000, 256, 384, 129, 700, 255]
+    lens_k = [max(0, n + shift) for n in lens_q]
+    inp = make_inputs(lens_q, lens_k, 2, 2, 128, 128, "bf16", seed=70 + shift % 7)
+    causal = mask == "causal"
+    wl = 300 if mask == "window" else -1
+    out, lse = run_gpu(inp, causal=causal, window_left=wl, num_splits=1, guard_rows=1)
+    assert fa.fa_debug_last_kernel() == fa.FA_KID_UMMA2_PERSISTENT
+    o_ref, l_ref = reference(inp, 0.0, causal, wl)
+    assert_close(inp, out, lse, o_ref, l_ref)
+    out2, lse2 = run_gpu(inp, causal=causal, window_left=wl, num_splits=1, guard_rows=1,
+                         flags=fa.FA_KERNEL_UMMA2)
+    assert np.array_equal(out, out2, equal_nan=True) and np.array_equal(lse, lse2, equal_nan=True)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_persistent_prefill_out_not_32_byte_aligned(causal):
     """The persistent kernel writes O rows in 32-byte pieces, so an O that

@@ -457,6 +457,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       const int t = sq.q0 + i;
       const uint32_t o_addr = tmem + lane_base + C::TM_O;
+      const bool ws_wide = (reinterpret_cast<uintptr_t>(p.ws_o) & 31u) == 0;
 #pragma unroll
       for (int c = 0; c < DV / 32; ++c) {
         uint32_t o[32];
@@ -477,10 +478,18 @@ __global__ void __launch_bounds__(192, 1)
           const size_t slot = (size_t)b * p.max_seqlen_q + i;
           const size_t we = (((size_t)split * p.slots + slot) * p.h_q + h) * DV + c * 32;
           if (ws_o_ok(p, we, 32)) {
-            float4* dst = reinterpret_cast<float4*>(p.ws_o + we);
+            // whole 32-byte sectors when the workspace allows it (each
+            // thread writes its own row, so a store touches 32 rows)
+            if (ws_wide) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              dst[e] = make_float4(f[4 * e], f[4 * e + 1], f[4 * e + 2], f[4 * e + 3]);
+              for (int e = 0; e < 4; ++e)
+                st_global_32B(p.ws_o + we + 8 * e, reinterpret_cast<const uint32_t*>(f + 8 * e));
+            } else {
+              float4* dst = reinterpret_cast<float4*>(p.ws_o + we);
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                dst[e] = make_float4(f[4 * e], f[4 * e + 1], f[4 * e + 2], f[4 * e + 3]);
+            }
           }
         }
       }

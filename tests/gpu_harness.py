@@ -26,11 +26,12 @@ def device():
 
 
 def run_gpu(inp, scale=0.0, causal=False, window_left=-1, num_splits=0, flags=0,
-            with_lse=True, guard_rows=0, out_dtype=None, ws_guard=0, out_offset=0):
+            with_lse=True, guard_rows=0, out_dtype=None, ws_guard=0, out_offset=0, ws_offset=0):
     """Runs fa_fwd_splitkv_ex on `inp` (workloads.Inputs).  Output rows past
     the packed queries (guard_rows of them) and ws_guard floats past the
     workspace are filled with NaN sentinels and must stay untouched.  O starts
-    out_offset bytes into its allocation; the bytes before it must stay NaN."""
+    out_offset bytes into its allocation, the workspace ws_offset bytes into
+    its own; the bytes before either must stay NaN."""
     dev = device()
     q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
     cq, ck = inp.cu_seqlens_q.to(dev), inp.cu_seqlens_k.to(dev)
@@ -49,9 +50,12 @@ def run_gpu(inp, scale=0.0, causal=False, window_left=-1, num_splits=0, flags=0,
            if with_lse else None)
     ns_bytes = fa.fa_fwd_splitkv_workspace_size(inp.batch, inp.max_seqlen_q, inp.h_q, inp.h_kv,
                                                inp.d_v, num_splits)
-    ws = None
+    ws = ws_buf = None
+    ws_pre = ws_offset // 4
     if ns_bytes:
-        ws = torch.full((ns_bytes // 4 + ws_guard,), float("nan"), dtype=torch.float32, device=dev)
+        ws_buf = torch.full((ws_pre + ns_bytes // 4 + ws_guard,), float("nan"), dtype=torch.float32,
+                            device=dev)
+        ws = ws_buf[ws_pre:]
     dq = dk = dv = None
     if inp.dtype == "e4m3":
         dq = torch.tensor([inp.descale_q], dtype=torch.float32, device=dev)
@@ -66,6 +70,8 @@ def run_gpu(inp, scale=0.0, causal=False, window_left=-1, num_splits=0, flags=0,
         assert torch.isnan(ws[ns_bytes // 4:]).all(), "workspace guard overwritten"
     if pre:
         assert torch.isnan(out_buf[:pre].float()).all(), "bytes before O overwritten"
+    if ws_pre and ws_buf is not None:
+        assert torch.isnan(ws_buf[:ws_pre]).all(), "bytes before the workspace overwritten"
     return out.float().cpu().numpy(), (lse.cpu().numpy() if lse is not None else None)
 
 

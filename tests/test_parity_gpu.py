@@ -644,6 +644,23 @@ def test_persistent_prefill_mha_pair_last_block(mask, shift):
     assert np.array_equal(out, out2, equal_nan=True) and np.array_equal(lse, lse2, equal_nan=True)
 
 
+@pytest.mark.parametrize("shape", ["fp8_prefix", "gqa_decode"])
+def test_workspace_not_32_byte_aligned(shape):
+    """The one-tile kernel writes split partials as 32-byte stores when the
+    workspace is 32-byte aligned and as 16-byte stores otherwise: a workspace
+    16 bytes past a 32-byte boundary gives the oracle's result, bit for bit
+    the aligned call's, and leaves the bytes before it untouched."""
+    if shape == "fp8_prefix":
+        inp = make_inputs([70], [3000], 4, 4, 192, 128, "e4m3", seed=80)
+    else:
+        inp = make_inputs([1, 1, 1], [2500, 700, 4100], 16, 4, 128, 128, "bf16", seed=81)
+    out, lse = run_gpu(inp, num_splits=5, flags=fa.FA_KERNEL_UMMA, ws_offset=16, ws_guard=8)
+    o_ref, l_ref = reference(inp)
+    assert_close(inp, out, lse, o_ref, l_ref)
+    out2, lse2 = run_gpu(inp, num_splits=5, flags=fa.FA_KERNEL_UMMA)
+    assert np.array_equal(out, out2, equal_nan=True) and np.array_equal(lse, lse2, equal_nan=True)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_persistent_prefill_out_not_32_byte_aligned(causal):
     """The persistent kernel writes O rows in 32-byte pieces, so an O that

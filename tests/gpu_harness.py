@@ -123,13 +123,19 @@ def run_gpu_paged(inp, scale=0.0, causal=False, window_left=-1, num_splits=0, fl
     kc, vc = inp.k_cache.to(dev), inp.v_cache.to(dev)
     cq = inp.cu_seqlens_q.to(dev)
     sk, bt = inp.seqlens_k.to(dev), inp.block_table.to(dev)
-    out = torch.full((q.shape[0], inp.h_q, inp.d_v), float("nan"), dtype=q.dtype, device=dev)
+    out_dtype = torch.bfloat16 if inp.dtype == "e4m3" else q.dtype
+    out = torch.full((q.shape[0], inp.h_q, inp.d_v), float("nan"), dtype=out_dtype, device=dev)
     lse = torch.full((inp.h_q, q.shape[0]), float("nan"), dtype=torch.float32, device=dev)
     nbytes = fa.fa_fwd_splitkv_workspace_size(inp.batch, inp.max_seqlen_q, inp.h_q, inp.h_kv,
                                              inp.d_v, num_splits)
     ws = torch.empty(max(nbytes, 16) // 4, dtype=torch.float32, device=dev) if nbytes else None
+    dq = dk = dv = None
+    if inp.dtype == "e4m3":
+        dq = torch.tensor([inp.descale_q], dtype=torch.float32, device=dev)
+        dk = torch.tensor([inp.descale_k], dtype=torch.float32, device=dev)
+        dv = torch.tensor([inp.descale_v], dtype=torch.float32, device=dev)
     fa.fa_fwd_splitkv_paged(q, kc, vc, cq, sk, bt, inp.max_seqlen_q, out, lse, ws, scale, causal,
-                            window_left, num_splits, flags=flags)
+                            window_left, num_splits, dq, dk, dv, flags=flags)
     torch.cuda.synchronize()
     err = fa.fa_get_device_error(clear=True)
     assert err == 0, fa.fa_status_string(err)
@@ -140,4 +146,5 @@ def reference_paged(inp, scale=0.0, causal=False, window_left=-1):
     """The oracle on the paged cache gathered back into packed K/V."""
     k, v, cu_k = oracle.gather_paged_kv(inp.k_cache, inp.v_cache, inp.block_table, inp.seqlens_k)
     return oracle.attention_forward(inp.q, k, v, inp.cu_seqlens_q, cu_k, inp.h_q, inp.h_kv,
-                                    scale, causal, window_left)
+                                    scale, causal, window_left, inp.descale_q, inp.descale_k,
+                                    inp.descale_v)

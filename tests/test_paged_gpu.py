@@ -37,6 +37,30 @@ def test_paged_prefix_masks(kernel, mask):
     assert_close(inp, out, lse, o_ref, l_ref)
 
 
+@pytest.mark.parametrize("kernel", [fa.FA_KERNEL_SIMT, fa.FA_KERNEL_UMMA])
+@pytest.mark.parametrize("d_qk,page_size", [(192, 32), (192, 64), (128, 128)])
+def test_paged_fp8(kernel, d_qk, page_size):
+    """e4m3 K/V pages (d_v = 128) with a few queries per sequence, ragged key
+    counts and shuffled pages; bf16 output against the oracle."""
+    inp = make_paged_inputs([1, 3, 70], [1500, 333, 2100], 6, 6, d_qk, 128, page_size,
+                            dtype="e4m3", seed=25)
+    out, lse = run_gpu_paged(inp, num_splits=4, flags=kernel)
+    o_ref, l_ref = reference_paged(inp)
+    assert_close(inp, out, lse, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dtype,d", [("fp16", 64), ("bf16", 256)])
+def test_paged_other_head_dims(kernel, dtype, d):
+    """Head dims 64 (fp16) and 256 (bf16) through the page cursor, causal."""
+    if kernel == fa.FA_KERNEL_UMMA2 and d == 256:
+        pytest.skip("the two-tile kernel takes head dims up to 128")
+    inp = make_paged_inputs([2, 1, 9], [900, 64, 1700], 8, 2, d, d, 64, dtype=dtype, seed=26)
+    out, lse = run_gpu_paged(inp, causal=True, num_splits=3, flags=kernel)
+    o_ref, l_ref = reference_paged(inp, 0.0, True)
+    assert_close(inp, out, lse, o_ref, l_ref)
+
+
 def test_paged_equals_packed_path():
     """The same keys through the paged and the packed entry points agree."""
     from gpu_harness import run_gpu

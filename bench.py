@@ -472,9 +472,14 @@ def cpu_baseline(inp_cpu, budget_s=12.0, heads=2, causal=False, kind="hbm"):
     group = inp_cpu.h_q // inp_cpu.h_kv
     hs = list(range(heads))
     kvs = sorted({h // group for h in hs})
-    q = inp_cpu.q[:, hs]
-    k = inp_cpu.k[:, kvs]
-    v = inp_cpu.v[:, kvs]
+    def heads_of(x, idx):  # through bytes: CPU indexing of e4m3 tensors is not implemented
+        if x.dtype == torch.float8_e4m3fn:
+            return x.view(torch.uint8)[:, idx].view(x.dtype)
+        return x[:, idx]
+
+    q = heads_of(inp_cpu.q, hs)
+    k = heads_of(inp_cpu.k, kvs)
+    v = heads_of(inp_cpu.v, kvs)
     es = 1 if inp_cpu.dtype == "e4m3" else 2
     tq, tk = q.shape[0], k.shape[0]
     if kind == "tensor":
@@ -651,7 +656,10 @@ def main():
         unit = "TB/s"
         value = job_throughput(metric_b, world, ms_per_step)
 
-    # ---- end to end through the public call with host buffers
+    # ---- end to end with host buffers: packed K/V through the library's
+    # host-buffer call (fa_fwd_splitkv_host: the copies to and from the
+    # device are part of the call); paged K/V (no host-buffer call) copied
+    # around the device call
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
     q, k, v = case.copies[0]
     # the step's inputs: Q and cu_seqlens_q, and K/V with their index arrays
@@ -661,13 +669,29 @@ def main():
     h_lse = torch.empty(case.lse.shape, dtype=case.lse.dtype).pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in host_in)
     d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+    dev_buf = None
+    if paged:
+        def e2e_step():
+            for d_t, h_t in zip(dev_in, host_in):
+                d_t.copy_(h_t, non_blocking=True)
+            call(0, stream)
+            h_out.copy_(case.out, non_blocking=True)
+            h_lse.copy_(case.lse, non_blocking=True)
+    else:
+        hq, hcq, hk, hv, hck = host_in
+        h_dsc = [None] * 3
+        if inp.dtype == "e4m3":
+            h_dsc = [d.cpu().pin_memory() for d in (case.dq, case.dk, case.dv)]
+            h2d += 3 * 4
+        nbuf = fa.fa_fwd_splitkv_host_buffer_size(
+            inp.batch, hq.shape[0], hk.shape[0], inp.max_seqlen_q, inp.h_q, inp.h_kv, hq.shape[2],
+            inp.d_v, hq.dtype, h_out.dtype, args.num_splits)
+        dev_buf = torch.empty(nbuf, dtype=torch.uint8, device=dev)
 
-    def e2e_step():
-        for d_t, h_t in zip(dev_in, host_in):
-            d_t.copy_(h_t, non_blocking=True)
-        call(0, stream)
-        h_out.copy_(case.out, non_blocking=True)
-        h_lse.copy_(case.lse, non_blocking=True)
+        def e2e_step():
+            fa.fa_fwd_splitkv_host(hq, hk, hv, hcq, hck, inp.max_seqlen_q, h_out, h_lse, dev_buf,
+                                   0.0, causal, -1, args.num_splits, h_dsc[0], h_dsc[1], h_dsc[2],
+                                   kernel_flag, stream)
 
     e2e_step()
     torch.cuda.synchronize(dev)
@@ -681,7 +705,8 @@ def main():
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
     e2e_value = job_throughput(work_flops if kind == "tensor" else metric_b, world, e2e_ms)
-    del case, host_in
+    del case, host_in, e2e_step
+    dev_buf = None
     torch.cuda.empty_cache()
 
     peak_gbs, peak_src = measured_peaks()

@@ -232,6 +232,51 @@ FA_API int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v,
                                   const float* descale_v, int flags, void* stream);
 
 /*
+ * fa_fwd_splitkv_host -- the same forward pass on host buffers (no
+ * counterpart on the pages this library follows; an addition for callers
+ * whose inputs and outputs live in host memory, and the end-to-end call a
+ * benchmark times).  q, k, v, cu_seqlens_q, cu_seqlens_k and, for FA_E4M3
+ * inputs, descale_q/k/v (one float each) are read from HOST memory; out and
+ * lse (may be NULL) are written to HOST memory.  Layouts are those of
+ * fa_fwd_splitkv_ex.  Each transfer is one cudaMemcpyAsync on `stream` in
+ * stream order: the inputs, then the forward pass, then O and LSE.  The
+ * call returns once they are enqueued; synchronise the stream before
+ * reading out/lse or reusing an input buffer.  Page-locked host buffers make
+ * the copies asynchronous; pageable ones work, with each copy staged by the
+ * driver.
+ *
+ * device_buffer (device, 256-byte aligned, caller-owned, device_buffer_bytes
+ * at least fa_fwd_splitkv_host_buffer_size(...)) holds the device copies of
+ * the inputs, O, LSE and the split workspace; the call allocates nothing.
+ * Errors: FA_ERR_INVALID_ARG for invalid sizes or dtypes, a NULL or
+ * misaligned device_buffer, or a NULL host buffer that has bytes to copy;
+ * FA_ERR_WORKSPACE when device_buffer is too small (both before any copy);
+ * FA_ERR_CUDA when a copy cannot be enqueued; otherwise whatever
+ * fa_fwd_splitkv_ex returns for the device copies.
+ */
+FA_API int fa_fwd_splitkv_host(const void* q, const void* k, const void* v,
+                               const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                               int total_q, int total_k, int max_seqlen_q, int h_q, int h_kv,
+                               int d_qk, int d_v, float scale, int causal, int window_left,
+                               int num_splits, void* out, float* lse, void* device_buffer,
+                               size_t device_buffer_bytes, int in_dtype, int out_dtype,
+                               const float* descale_q, const float* descale_k,
+                               const float* descale_v, int flags, void* stream);
+
+/*
+ * fa_fwd_splitkv_host_buffer_size -- bytes of device buffer
+ * fa_fwd_splitkv_host needs for these sizes (no counterpart on the pages
+ * this library follows): 256-byte aligned regions for Q, K, V, the two
+ * offset arrays, the descales, O, LSE and the split workspace of
+ * fa_fwd_splitkv_workspace_size.  num_splits = 0 resolves the automatic
+ * count on the current device.  Returns 0 for invalid sizes or dtypes.
+ */
+FA_API size_t fa_fwd_splitkv_host_buffer_size(int batch, int total_q, int total_k,
+                                              int max_seqlen_q, int h_q, int h_kv, int d_qk,
+                                              int d_v, int in_dtype, int out_dtype,
+                                              int num_splits);
+
+/*
  * fa_fwd_splitkv_workspace_size -- bytes of workspace fa_fwd_splitkv_ex needs
  * for these sizes.  aiter PR "[FlyDSL] Enable FP8 FMHA split-K for short
  * cached-prefix queries" (review: automatic split-K "plus a per-call fp32

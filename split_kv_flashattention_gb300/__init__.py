@@ -25,7 +25,7 @@ __all__ = [
     "fa_get_device_error", "fa_status_string", "fa_version", "forward",
     "FA_KERNEL_AUTO", "FA_KERNEL_SIMT", "FA_KERNEL_UMMA", "FA_KERNEL_UMMA2", "FA_RUN_PARTIAL_ONLY",
     "FA_RUN_COMBINE_ONLY", "DTYPE_CODES", "fa_fwd_splitkv_noalloc", "NOALLOC_SCRATCH_BYTES",
-    "fa_fwd_splitkv_paged",
+    "fa_fwd_splitkv_paged", "fa_fwd_splitkv_host", "fa_fwd_splitkv_host_buffer_size",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libfa_splitkv.so")
@@ -42,7 +42,7 @@ EXPORTED = (
     "fa_fwd_splitkv_ex", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace_size", "fa_plan",
     "fa_debug_split_ranges", "fa_get_device_error", "fa_status_string", "fa_version",
     "fa_fwd_splitkv_noalloc", "fa_fwd_splitkv_paged", "fa_debug_wait_timeout",
-    "fa_debug_last_kernel",
+    "fa_debug_last_kernel", "fa_fwd_splitkv_host", "fa_fwd_splitkv_host_buffer_size",
 )
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -92,6 +92,13 @@ def library() -> ctypes.CDLL:
         _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
         _c_int, _c_int, _c_int, _c_float, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_size, _c_int,
         _c_int, _vp, _vp, _vp, _c_int, _vp]
+    lib.fa_fwd_splitkv_host.restype = _c_int
+    lib.fa_fwd_splitkv_host.argtypes = [
+        _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+        _c_float, _c_int, _c_int, _c_int, _vp, _vp, _vp, _c_size, _c_int, _c_int, _vp, _vp, _vp,
+        _c_int, _vp]
+    lib.fa_fwd_splitkv_host_buffer_size.restype = _c_size
+    lib.fa_fwd_splitkv_host_buffer_size.argtypes = [_c_int] * 11
     lib.fa_fwd_splitkv_workspace_size.restype = _c_size
     lib.fa_fwd_splitkv_workspace_size.argtypes = [_c_int] * 6
     lib.fa_plan.restype = _c_int
@@ -151,8 +158,9 @@ _F32 = (torch.float32,)
 
 
 def _check_forward_args(q, k, v, cu_seqlens_q, seqlens_k_name, seqlens_k, out, lse, workspace,
-                        descales, kv_ndim=3):
-    """Shapes, dtypes, contiguity and device of a forward call's tensors."""
+                        descales, kv_ndim=3, on_host=False):
+    """Shapes, dtypes, contiguity and device of a forward call's tensors (all
+    in host memory when on_host)."""
     _tensor(q, "q", dtypes=_INPUT_DTYPES)
     _tensor(k, "k", dtypes=(q.dtype,))
     _tensor(v, "v", dtypes=(q.dtype,))
@@ -176,6 +184,13 @@ def _check_forward_args(q, k, v, cu_seqlens_q, seqlens_k_name, seqlens_k, out, l
         _tensor(d, name, dtypes=_F32, optional=True)
         if d is not None and d.numel() < 1:
             raise ValueError(f"{name} must hold one float32 value")
+    if on_host:
+        named = dict(q=q, k=k, v=v, cu_seqlens_q=cu_seqlens_q, **{seqlens_k_name: seqlens_k},
+                     out=out, lse=lse, **descales)
+        for name, t in named.items():
+            if t is not None and t.is_cuda:
+                raise ValueError(f"{name} must be a host (CPU) tensor, got {t.device}")
+        return
     _on_device(q, k=k, v=v, cu_seqlens_q=cu_seqlens_q, **{seqlens_k_name: seqlens_k}, out=out,
                lse=lse, workspace=workspace, **descales)
 
@@ -245,6 +260,47 @@ def fa_debug_split_ranges(cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal:
                                            tile_queries, _ptr(out), _stream(stream)),
            "fa_debug_split_ranges")
     return out
+
+
+def fa_fwd_splitkv_host_buffer_size(batch: int, total_q: int, total_k: int, max_seqlen_q: int,
+                                    h_q: int, h_kv: int, d_qk: int, d_v: int, in_dtype,
+                                    out_dtype, num_splits: int = 0) -> int:
+    """Bytes of device buffer fa_fwd_splitkv_host needs (0: invalid sizes);
+    in_dtype/out_dtype are torch dtypes."""
+    return int(library().fa_fwd_splitkv_host_buffer_size(
+        batch, total_q, total_k, max_seqlen_q, h_q, h_kv, d_qk, d_v, DTYPE_CODES[in_dtype],
+        DTYPE_CODES[out_dtype], num_splits))
+
+
+def fa_fwd_splitkv_host(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, out, lse,
+                        device_buffer, scale: float = 0.0, causal: bool = False,
+                        window_left: int = -1, num_splits: int = 0, descale_q=None,
+                        descale_k=None, descale_v=None, flags: int = FA_KERNEL_AUTO,
+                        stream=None):
+    """Calls fa_fwd_splitkv_host: q, k, v, the offsets, out, lse and the
+    descales are host (CPU) tensors, pinned for asynchronous copies;
+    device_buffer is a CUDA tensor of at least
+    fa_fwd_splitkv_host_buffer_size(...) bytes, 256-byte aligned.  The copies
+    and the forward pass are enqueued on `stream`: synchronise it before
+    reading out or lse."""
+    _check_forward_args(q, k, v, cu_seqlens_q, "cu_seqlens_k", cu_seqlens_k, out, lse, None,
+                        dict(descale_q=descale_q, descale_k=descale_k, descale_v=descale_v),
+                        on_host=True)
+    _tensor(device_buffer, "device_buffer")
+    if not device_buffer.is_cuda:
+        raise ValueError("device_buffer must be a CUDA tensor (device memory)")
+    total_q, h_q, d_qk = q.shape
+    total_k, h_kv, _ = k.shape
+    d_v = v.shape[2]
+    batch = cu_seqlens_q.numel() - 1
+    nbytes = device_buffer.numel() * device_buffer.element_size()
+    st = library().fa_fwd_splitkv_host(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, total_q,
+        total_k, max_seqlen_q, h_q, h_kv, d_qk, d_v, float(scale), int(causal), int(window_left),
+        int(num_splits), _ptr(out), _ptr(lse), _ptr(device_buffer), nbytes, DTYPE_CODES[q.dtype],
+        DTYPE_CODES[out.dtype], _ptr(descale_q), _ptr(descale_k), _ptr(descale_v), int(flags),
+        _stream(stream))
+    _check(st, "fa_fwd_splitkv_host")
 
 
 def fa_fwd_splitkv_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, out, lse=None,

@@ -45,6 +45,12 @@ int main(void) {
                           (void*)dev, NULL, NULL, 0, FA_BF16, FA_BF16, NULL, NULL, NULL,
                           FA_KERNEL_AUTO, NULL) == FA_ERR_UNSUPPORTED);
   CHECK(fa_debug_last_kernel() == FA_KID_NONE);
+  /* host-buffer call: its device-buffer size, and a missing buffer refused before any copy */
+  CHECK(fa_fwd_splitkv_host_buffer_size(1, 1, 64, 1, 4, 4, 128, 128, FA_BF16, FA_BF16, 2) > 0);
+  CHECK(fa_fwd_splitkv_host_buffer_size(1, 1, 64, 1, 6, 4, 128, 128, FA_BF16, FA_BF16, 2) == 0);
+  CHECK(fa_fwd_splitkv_host(dev, dev, dev, cu, cu, 1, 1, 64, 1, 4, 4, 128, 128, 0.f, 0, -1, 2,
+                            (void*)dev, NULL, NULL, 0, FA_BF16, FA_BF16, NULL, NULL, NULL, 0,
+                            NULL) == FA_ERR_INVALID_ARG);
 
   puts("c client ok");
   return 0;

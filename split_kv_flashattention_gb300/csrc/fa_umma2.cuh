@@ -32,6 +32,22 @@
 
 namespace fa {
 
+// Non-blocking test of an mbarrier phase (no suspension).  A test or wait
+// on a phase that has completed still takes about 70 cycles; several tests
+// issued back to back overlap those latencies, where the same number of
+// waits in a row would add them up on the MMA thread's path.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // The shared-memory descriptor of fa_ptx.cuh (smem_desc_sw128) in two words.  For fixed offsets only the low word
 // (start address and leading byte offset) depends on the address, so an
 // issue loop keeps the high word in one register and steps the low word:
@@ -315,10 +331,22 @@ __global__ void __launch_bounds__(384, 1)
       }
       for (int j = 0; ok && j < nblk; ++j) {
         for (int t = 0; t < ntiles; ++t) {
-          ok = mbar_wait(p_ready + 8 * t, j & 1, p.err, abort_flag);
-          if (ok && t == 0) ok = mbar_wait(v_full + 8 * (j % VS), (j / VS) & 1, p.err, abort_flag);
-          if (ok && t == 0 && j + 1 < nblk)
-            ok = mbar_wait(k_full + 8 * ((j + 1) % KS), ((j + 1) / KS) & 1, p.err, abort_flag);
+          // slot A's P, V(j) and K(j+1) tested together first (their
+          // latencies overlap); waited for one by one only when one is not
+          // complete
+          bool ready = false;
+          if (t == 0)
+            ready = mbar_test_wait(p_ready, j & 1) &
+                    mbar_test_wait(v_full + 8 * (j % VS), (j / VS) & 1) &
+                    (j + 1 >= nblk ||
+                     mbar_test_wait(k_full + 8 * ((j + 1) % KS), ((j + 1) / KS) & 1));
+          if (!ready) {
+            ok = mbar_wait(p_ready + 8 * t, j & 1, p.err, abort_flag);
+            if (ok && t == 0)
+              ok = mbar_wait(v_full + 8 * (j % VS), (j / VS) & 1, p.err, abort_flag);
+            if (ok && t == 0 && j + 1 < nblk)
+              ok = mbar_wait(k_full + 8 * ((j + 1) % KS), ((j + 1) / KS) & 1, p.err, abort_flag);
+          }
           if (!ok) break;
           tc_fence_after();
           issue_pv(t, j);

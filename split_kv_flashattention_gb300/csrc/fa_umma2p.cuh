@@ -481,11 +481,23 @@ __global__ void __launch_bounds__(384, 1)
             const bool last = j + 1 == T.nblk;
             uint32_t s0m = 0;  // slots given the next tile's S(0)
             for (int t = 0; t < ntiles; ++t) {
-              ok = mbar_wait(p_ready + 8 * t, (pcb >> t) & 1, p.err, abort_flag);
+              // Slot A's P, V(j) and K(j+1) are usually all there by now: the
+              // three phases are tested together (each test takes about 70
+              // cycles, and back to back they overlap), and waited for one
+              // by one only when one is not complete.
+              bool ready = false;
+              if (t == 0)
+                ready = mbar_test_wait(p_ready, pcb & 1) &
+                        mbar_test_wait(v_full + 8 * vst, (gv / VS) & 1) &
+                        (last || mbar_test_wait(k_full + 8 * (gk % KS), (gk / KS) & 1));
+              if (!ready) {
+                ok = mbar_wait(p_ready + 8 * t, (pcb >> t) & 1, p.err, abort_flag);
+                if (ok && t == 0)
+                  ok = mbar_wait(v_full + 8 * vst, (gv / VS) & 1, p.err, abort_flag);
+                if (ok && t == 0 && !last)
+                  ok = mbar_wait(k_full + 8 * (gk % KS), (gk / KS) & 1, p.err, abort_flag);
+              }
               pcb ^= 1u << t;
-              if (ok && t == 0) ok = mbar_wait(v_full + 8 * vst, (gv / VS) & 1, p.err, abort_flag);
-              if (ok && t == 0 && !last)
-                ok = mbar_wait(k_full + 8 * (gk % KS), (gk / KS) & 1, p.err, abort_flag);
               // the previous tile's O in this slot has been read out of TMEM
               if (ok && j == 0 && ((odv >> t) & 1))
                 ok = mbar_wait(o_free + 8 * t, ((odb >> t) & 1) ^ 1u, p.err, abort_flag);

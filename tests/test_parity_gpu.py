@@ -408,6 +408,19 @@ def test_full_long_decode_sampled_heads():
     assert np.isfinite(out).all() and np.isfinite(lse).all()
 
 
+def test_full_long_decode_split_sweep():
+    """The long decode at every split count the benchmark times (FA4 page,
+    "Benchmarks": 1 to 128 splits), 2 of 32 heads checked against the
+    oracle for each."""
+    inp = workload("long_decode", device="cuda")
+    heads = [3, 26]
+    o_ref, l_ref = reference(inp, heads=heads)
+    for ns in (1, 2, 4, 8, 16, 32, 64, 128):
+        out, lse = run_gpu(inp, num_splits=ns)
+        assert_close(inp, out, lse, o_ref, l_ref, heads=heads)
+        assert np.isfinite(out).all() and np.isfinite(lse).all(), ns
+
+
 def test_full_gqa_decode_varlen():
     inp = workload("gqa_decode", device="cuda")
     assert sum(gqa_decode_lengths(0)) == int(inp.cu_seqlens_k[-1])
